@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 MoE FFN layer forward pass (tokens/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|...]
+    python bench.py --impl reference ...     # the CPU oracle, timed on the host cores
+
+One step = one pass of the whole layer (route -> permute -> expert FFN +
+shared expert -> combine) over one batch of T synthetic tokens whose inputs
+and weights are already resident in HBM.  The timed region is exactly K steps
+between a barrier + device synchronisation on each side; every stage is
+bracketed by CUDA events on the launching stream, which gives the per-stage
+times the roofline uses.  The end-to-end figure repeats the measurement
+through the public call with host buffers (pinned x in, y out, copies inside
+the timed region).
+
+Multi-GPU (torchrun, one process per GPU): the layer is per-token
+independent, so ranks are independent replicas of the same workload (weak
+scaling, no collective on the data path); value = tokens of all ranks / the
+slowest rank's time.  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at T=8192 and T=64; % of FP8-TC / HBM roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOAD_TEXT = {
+    "decode": "decode step: T=64 tokens, d_model=4096, 128 experts, top-6 softmax routing, SwiGLU f=1024, "
+              "1 shared expert f=1024, FP8 E4M3 weights with per-channel fp32 scales, bf16 x",
+    "prefill": "chunked prefill: T=8192 tokens (32 x 256), d_model=4096, 128 experts, top-6, SwiGLU f=1024, "
+               "1 shared expert f=1024, FP8 E4M3 weights, bf16 x",
+    "skew": "skewed routing: T=4096, Zipf(1.2)-biased router (hottest expert ~8x mean, 4+ empty), FP8 weights",
+    "100b_decode": "100B-style decode: T=64, d_model=4096, 128 experts, top-8, SwiGLU f=2048, NVFP4 weights",
+    "100b_prefill": "100B-style prefill: T=8192, d_model=4096, 128 experts, top-8, SwiGLU f=2048, NVFP4 weights",
+    "tiny": "tiny: T=32, d_model=128, 128 experts, top-6, f=64, all fp32",
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def weight_bytes_per_expert(cfg):
+    d, f = cfg.d, cfg.f
+    n = 3 * d * f
+    if cfg.w_dtype == "e4m3":
+        return n + 4 * (2 * f + d)
+    if cfg.w_dtype == "nvfp4":
+        return n // 2 + n // 16 + 8
+    return 4 * n
+
+
+def shared_weight_bytes(cfg):
+    d, fs = cfg.d, cfg.fs
+    n = 3 * d * fs
+    if cfg.w_dtype == "e4m3":
+        return n + 4 * (2 * fs + d)
+    if cfg.w_dtype == "nvfp4":
+        return n // 2 + n // 16 + 8
+    return 4 * n
+
+
+def algorithmic(cfg, counts):
+    """Bytes and FLOPs of one layer pass (activated work only).
+
+    Layer bytes: weights of the experts that received tokens + shared-expert
+    weights + router weights + x (read) + y (fp32, written).
+    Expert-FFN stage bytes (the dominant stage): active expert weights +
+    shared weights + x + its outputs out_perm [T*k, d] and shared_out [T, d]
+    (fp32).  FLOPs: 6*d*f per routed pair + 6*d*f_s per token (+ router).
+    """
+    active = int((counts > 0).sum())
+    xb = cfg.T * cfg.d * (2 if cfg.x_dtype == "bf16" else 4)
+    wexp = active * weight_bytes_per_expert(cfg) + shared_weight_bytes(cfg)
+    P = cfg.T * cfg.k
+    ffn_bytes = wexp + xb + 4 * (P + cfg.T) * cfg.d
+    layer_bytes = wexp + 4 * cfg.E * cfg.d + xb + 4 * cfg.T * cfg.d
+    ffn_flops = 6.0 * cfg.d * cfg.f * P + 6.0 * cfg.d * cfg.fs * cfg.T
+    layer_flops = ffn_flops + 2.0 * cfg.T * cfg.d * cfg.E
+    return dict(active=active, ffn_bytes=ffn_bytes, layer_bytes=layer_bytes, ffn_flops=ffn_flops,
+                layer_flops=layer_flops)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def time_oracle(inp, budget_s, chunk=2):
+    """Oracle tokens/s on a bounded sample: tokens in chunks until the budget."""
+    import oracle
+    T = inp.cfg.T
+    done, t0 = 0, time.perf_counter()
+    while done < T:
+        n = min(chunk, T - done)
+        oracle.layer_forward_tokens(inp, range(done, done + n))
+        done += n
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done / el, done, el
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ traffic record
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "top_routed_expert_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as fh:
+            h.update(fn.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, kernel):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        rec = json.load(fh)
+    r = rec.get(workload, {})
+    if r.get("kernel") != kernel or r.get("source_hash") != source_hash():
+        return None
+    return r.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ arms
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import moe_synth
+    inp = moe_synth.make_inputs(args.workload)
+    chunk = 2
+    for _ in range(args.warmup):
+        time_oracle(inp, 0.0, chunk)
+    t0 = time.perf_counter()
+    toks = 0
+    for _ in range(args.steps):
+        _, n, _ = time_oracle(inp, 0.0, chunk)
+        toks += n
+    el = time.perf_counter() - t0
+    v = toks / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/d) weights quantised to the stored format)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "T": inp.cfg.T},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"each step: the fp64 CPU oracle on {chunk} of the {inp.cfg.T} tokens "
+                                   f"(routing + every expert they use, dequantised one at a time)"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import moe_synth
+    import top_routed_expert_gb300 as moe
+    from top_routed_expert_gb300 import abi
+    from top_routed_expert_gb300.layer import MoELayer, _to_dev
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.build()
+    inp = moe_synth.make_inputs(args.workload)
+    cfg = inp.cfg
+    layer = MoELayer(inp, device=dev, flags=abi.MOE_FLAG_SIMT_FFN if args.simt else 0)
+    x = _to_dev(inp.x, dev)
+    T, k, E, d = cfg.T, cfg.k, cfg.E, cfg.d
+    P = T * k
+    c = layer.config()
+    ws = layer.workspace()
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(P, dtype=torch.int32, device=dev)
+    row_of = torch.empty(P, dtype=torch.int32, device=dev)
+    out_perm = torch.empty((P, d), dtype=torch.float32, device=dev)
+    shared = torch.empty((T, d), dtype=torch.float32, device=dev)
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        abi.moe_route(c, x, layer.w_router, layer.bias, ids, w, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        abi.moe_permute(c, ids, offs, sp, row_of, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        abi.moe_expert_ffn(c, x, w, offs, sp, layer.weights, out_perm, shared, ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        abi.moe_combine(c, out_perm, row_of, shared, y, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    st = abi.moe_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {abi.STATUS.get(st, st)}")
+    counts = np.diff(offs.cpu().numpy())
+    alg = algorithmic(cfg, counts)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    launches0 = abi.moe_launch_count()
+    barrier()
+    with ClockSampler(gpu_index) as clk:
+        for i in range(args.steps):
+            step(evs[i])
+        barrier()
+    launches = abi.moe_launch_count() - launches0
+    st = abi.moe_get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {abi.STATUS.get(st, st)}")
+    total_ms = evs[0][0].elapsed_time(evs[-1][4])
+    stage_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps
+                for j, name in enumerate(["route", "permute", "expert_ffn", "combine"])}
+    ms_step = total_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # end to end through the public call, host buffers
+    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_host.copy_(x)
+    y_host = torch.empty((T, d), dtype=torch.float32, pin_memory=True)
+    x_stage = torch.empty_like(x)
+    y_stage = torch.empty((T, d), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        layer.forward_host(x_host, y_host, x_stage, y_stage, stream)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.forward_host(x_host, y_host, x_stage, y_stage, stream)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    fp8_tf = 2.0 * peaks["bf16_tflops"]          # measured bf16 x nominal fp8/bf16 ratio of 2
+    ffn_s = stage_ms["expert_ffn"] / 1e3
+    t_hbm = alg["ffn_bytes"] / (hbm * 1e9)
+    t_tc = alg["ffn_flops"] / (fp8_tf * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": alg["ffn_bytes"] / ffn_s / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": alg["ffn_flops"] / ffn_s / 1e12, "peak": fp8_tf, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = "moe_expert_ffn (grouped SwiGLU GEMMs + shared expert)"
+    roof["peak_source"] = f"{peak_src} ({'HBM copy' if roof['bound'] == 'hbm' else 'bf16 cuBLAS x2 for FP8'})"
+    roof["traffic"] = recorded_traffic(args.workload, roof["kernel"])
+    t_layer_roof = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (fp8_tf * 1e12))
+    value = world * T / (ms_step / 1e3)
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, n, el = time_oracle(inp, args.cpu_budget)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+               "sample": f"{n} of the {T} tokens of this workload through the fp64 CPU oracle ({el:.1f} s)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp32-accumulate; FP8/NVFP4 weights, bf16 x" if not args.simt else "f32",
+        "data": "synthetic (seeded N(0,1) bf16 activations, N(0,1/d) weights quantised to the stored format)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "T": T, "d_model": d, "n_experts": E, "top_k": k,
+                   "d_ff": cfg.f, "d_ff_shared": cfg.fs, "weights": cfg.w_dtype,
+                   "ffn_path": "simt" if args.simt else "default",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: expert weights %.2f GB per pass" % (alg["ffn_bytes"] / 1e9)},
+        "stages_ms": stage_ms,
+        "roofline": roof,
+        "layer_roofline_frac": t_layer_roof / (ms_step / 1e3),
+        "active_experts": alg["active"],
+        "clocks": clk.summary(),
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": T * d * 4},
+        "gpu_launches": int(launches),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="decode")
+    ap.add_argument("--simt", action="store_true", help="force the CUDA-core expert kernels")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) MoE FFN layer forward pass.
+ *
+ * The layer (NVIDIA technical blog "How NVIDIA extreme hardware-software
+ * co-design delivered a large inference boost for Sarvam AI's sovereign
+ * models", section "Scaling multilingual sovereign AI with MoE" and Table 1):
+ * 128 routed experts with top-k routing (k = 6 for the 30B shape, 8 for the
+ * 100B shape), SwiGLU expert FFNs on FP8 or NVFP4 weights, one always-on
+ * shared expert, and a per-token weighted combine.
+ *
+ *   logits  L[t,e] = x[t,:] . W_r[e,:] (+ b[e])
+ *   ids[t]  = the k experts of largest L[t,e]; equal logits -> lower index first
+ *   w[t,j]  = softmax over all experts, restricted to ids[t], renormalised
+ *           = exp(L[t,ids_j] - L[t,ids_0]) / sum_i exp(L[t,ids_i] - L[t,ids_0])
+ *   FFN_e(v) = W2_e ( silu(Wg_e v) * (Wu_e v) ),  W13_e = [Wg_e ; Wu_e]
+ *   y[t]    = FFN_shared(x[t]) + sum_j w[t,j] FFN_{ids[t,j]}(x[t])
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never frees or retains them, never copies weights, and allocates no
+ *    device memory.  Scratch memory comes from the caller's workspace
+ *    (`ws`, at least moe_workspace_bytes(cfg) bytes, 256-byte aligned).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and performs no host synchronisation.
+ *  - Argument, shape, alignment and workspace errors are detected on the host
+ *    before anything is launched and returned synchronously.  Launch failures
+ *    return MOE_ERR_CUDA.  Faults detected on the device (an index out of
+ *    range, a bounded wait that ran out, a non-finite logit row) are recorded
+ *    in a per-device status word and returned by moe_get_device_status().
+ *    Nothing traps, aborts or throws across this boundary.
+ *  - Layouts are row-major with the last index contiguous.  Pair p = t*k + j
+ *    names slot j of token t.
+ *  - The device must be compute capability 10.3 (GB300); otherwise every
+ *    launching call returns MOE_ERR_ARCH.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,      /* null / misaligned pointer, bad shape        */
+  MOE_ERR_UNSUPPORTED = 2,      /* valid but not implemented combination       */
+  MOE_ERR_WORKSPACE = 3,        /* ws NULL or smaller than moe_workspace_bytes */
+  MOE_ERR_CUDA = 4,             /* a CUDA runtime / launch error               */
+  MOE_ERR_DEVICE_TIMEOUT = 5,   /* a bounded device-side wait ran out          */
+  MOE_ERR_DEVICE_BOUNDS = 6,    /* an index read on the device was out of range */
+  MOE_ERR_ARCH = 7,             /* current device is not sm_103                */
+  MOE_ERR_DEVICE_NONFINITE = 8  /* a router row had no finite logit            */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtype_t;
+
+/* Flags (moe_config_t.flags). */
+#define MOE_FLAG_SIMT_FFN 0x1u     /* run the expert FFN on the CUDA-core kernels */
+
+typedef struct {
+  int32_t T;            /* tokens, >= 0 (0 is a no-op)                          */
+  int32_t d_model;      /* hidden size d: multiple of 128, <= 16384             */
+  int32_t n_experts;    /* E: 1..256                                            */
+  int32_t top_k;        /* k: 1..min(E,16)                                      */
+  int32_t d_ff;         /* routed expert width f: multiple of 64                */
+  int32_t d_ff_shared;  /* shared expert width f_s: multiple of 64              */
+  int32_t x_dtype;      /* MOE_F32 or MOE_BF16                                  */
+  int32_t w_dtype;      /* MOE_F32, MOE_E4M3 or MOE_NVFP4 (expert + shared)     */
+  int32_t y_dtype;      /* MOE_F32 or MOE_BF16                                  */
+  uint32_t flags;       /* MOE_FLAG_*                                           */
+} moe_config_t;
+
+/*
+ * Expert weights in their stored formats (device pointers).
+ *   w13 : [E][2f][d]   rows 0..f-1 = gate (Wg), rows f..2f-1 = up (Wu)
+ *   w2  : [E][d][f]    down projection
+ *   s13 : [2f_s][d], s2 : [d][f_s]   shared expert, same formats
+ * Per format:
+ *   MOE_F32  : float values; *_scale and *_gscale unused (NULL).
+ *   MOE_E4M3 : uint8 FP8 E4M3 codes; *_scale = float per output row
+ *              (w13_scale [E][2f], w2_scale [E][d], s13_scale [2f_s],
+ *              s2_scale [d]); value = e4m3(code) * scale[row].
+ *   MOE_NVFP4: uint8, two E2M1 codes per byte along the K (last) axis, element
+ *              2i in the low nibble (w13 [E][2f][d/2] ...); *_scale = uint8
+ *              E4M3 codes, one per 16 consecutive K elements
+ *              (w13_scale [E][2f][d/16] ...); *_gscale = float per expert
+ *              ([E] for w13/w2, one float for s13/s2);
+ *              value = e2m1(code) * e4m3(block scale) * gscale.
+ * Source of the formats: the Sarvam summary page (peacm.com news/791474,
+ * section 2.1, FP8 expert weights) and the Sarvam blog's Blackwell section
+ * (NVFP4 weights).
+ */
+typedef struct {
+  const void* w13; const void* w13_scale; const float* w13_gscale;
+  const void* w2;  const void* w2_scale;  const float* w2_gscale;
+  const void* s13; const void* s13_scale; const float* s13_gscale;
+  const void* s2;  const void* s2_scale;  const float* s2_gscale;
+} moe_weights_t;
+
+typedef void* moe_stream_t;   /* a cudaStream_t */
+
+/* ABI version of the loaded library (MOE_ABI_VERSION at build time). */
+int moe_abi_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_str(moe_status_t s);
+
+/*
+ * Workspace bytes that moe_permute, moe_expert_ffn and moe_layer_forward
+ * need for this configuration (the maximum of the three).  Returns 0 for an
+ * invalid configuration.  The workspace holds no state between calls.
+ */
+size_t moe_workspace_bytes(const moe_config_t* cfg);
+
+/*
+ * Fused router: logits, softmax restricted to the top k, top-k selection.
+ * Sarvam blog, Table 1 row "Router logits and TopK" and the "MoE routing"
+ * paragraph (one fused kernel for logit computation and selection); Sarvam
+ * summary section 3.1 (the kernel writes expert indices and scores
+ * directly); InferX page section 3.3 (int32 indices, fp32 weights).
+ *   x           [T][d] (cfg->x_dtype)
+ *   w_router    [E][d] float
+ *   expert_bias [E] float added to the logits before selection, or NULL
+ *   topk_ids    [T][k] int32 out: experts in descending logit order, ties to
+ *               the lower index
+ *   topk_w      [T][k] float out: renormalised gates (sum to one per token)
+ * Uses no workspace.
+ */
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const float* w_router,
+                       const float* expert_bias, int32_t* topk_ids, float* topk_w,
+                       moe_stream_t stream);
+
+/*
+ * Permutation of the T*k (token, slot) pairs into per-expert groups, the
+ * token grouping that feeds the grouped expert GEMM (Sarvam blog, section on
+ * the H100 baseline: expert parallelism "uses grouped GEMM kernels").
+ *   topk_ids       [T][k] int32 in: values in [0, E); an out-of-range id is
+ *                  skipped and recorded as MOE_ERR_DEVICE_BOUNDS
+ *   expert_offsets [E+1] int32 out: exclusive prefix sum of per-expert counts
+ *   sorted_pair    [T*k] int32 out: pairs p = t*k+j ordered by (expert, p)
+ *   row_of         [T*k] int32 out: inverse of sorted_pair
+ */
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids,
+                         int32_t* expert_offsets, int32_t* sorted_pair, int32_t* row_of,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Routed experts (grouped SwiGLU GEMMs) and the shared expert.
+ * Sarvam blog, Table 1 rows "Routed expert compute" and "Shared expert
+ * compute"; section "Scaling multilingual sovereign AI with MoE" (shared
+ * expert design).
+ *   x              [T][d] (cfg->x_dtype)
+ *   topk_w         [T][k] float gates (from moe_route)
+ *   expert_offsets [E+1], sorted_pair [T*k] (from moe_permute)
+ *   out_perm       [T*k][d] float out: row r = topk_w[p] * FFN_e(x[t]) for
+ *                  p = sorted_pair[r] = t*k+j routed to expert e
+ *   shared_out     [T][d] float out: FFN_shared(x[t])
+ */
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float* topk_w,
+                            const int32_t* expert_offsets, const int32_t* sorted_pair,
+                            const moe_weights_t* weights, float* out_perm, float* shared_out,
+                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Deterministic combine: y[t] = shared_out[t] + sum_{j=0..k-1} out_perm[row_of[t*k+j]],
+ * added in slot order j (Sarvam summary section 2.1: shared plus routed
+ * experts).  y is [T][d] in cfg->y_dtype.  Uses no workspace.
+ */
+moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const int32_t* row_of,
+                         const float* shared_out, void* y, moe_stream_t stream);
+
+/*
+ * The whole layer: route -> permute -> expert FFN (+ shared) -> combine, all
+ * on `stream` with no host synchronisation.  topk_ids_opt / topk_w_opt /
+ * expert_offsets_opt, when not NULL, receive copies of the routing results.
+ */
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const float* w_router,
+                               const float* expert_bias, const moe_weights_t* weights, void* y,
+                               int32_t* topk_ids_opt, float* topk_w_opt,
+                               int32_t* expert_offsets_opt, void* ws, size_t ws_bytes,
+                               moe_stream_t stream);
+
+/*
+ * Number of kernels this library has launched in this process so far
+ * (diagnostics: lets a caller count the launches of a timed region).
+ */
+uint64_t moe_launch_count(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS,
+ * MOE_ERR_DEVICE_NONFINITE, or MOE_ERR_CUDA if the synchronisation failed.
+ */
+moe_status_t moe_get_device_status(moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,218 @@
+"""GPU parity of the whole layer and of each ABI call against the CPU oracle.
+
+Small shapes are compared element by element; the full-size workloads are
+compared on every token's routing and on a sample of tokens' outputs (the
+oracle computes those one expert at a time)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+import oracle
+from top_routed_expert_gb300 import abi
+from top_routed_expert_gb300.layer import MoELayer
+
+from .gpu_util import (check_output, check_routing, device_x, run_layer, sample_tokens, workload)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [pytest.param(0, id="default"), pytest.param(abi.MOE_FLAG_SIMT_FFN, id="simt")]
+
+
+@pytest.mark.parametrize("flags", PATHS)
+@pytest.mark.parametrize("name", ["tiny", "decode", "100b_decode"])
+def test_full_workload_elementwise(name, flags):
+    inp = workload(name)
+    _, _, y, ids, w, offs = run_layer(inp, flags)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids)
+
+
+@pytest.mark.parametrize("flags", PATHS)
+@pytest.mark.parametrize("name", ["prefill", "skew", "100b_prefill"])
+def test_full_workload_sampled(name, flags):
+    inp = workload(name)
+    _, _, y, ids, w, offs = run_layer(inp, flags)
+    check_routing(inp, ids, w, offs)
+    # sample includes tokens routed to the hottest expert
+    toks = set(sample_tokens(inp.cfg.T, 48).tolist())
+    hot = np.bincount(ids.reshape(-1), minlength=inp.cfg.E).argmax()
+    toks |= set(np.nonzero((ids == hot).any(1))[0][:16].tolist())
+    check_output(inp, y, ids, np.array(sorted(toks)))
+    assert np.all(np.isfinite(y))
+
+
+@pytest.mark.parametrize("flags", PATHS)
+@pytest.mark.parametrize("w_dtype", ["f32", "e4m3", "nvfp4"])
+@pytest.mark.parametrize("x_dtype", ["f32", "bf16"])
+def test_ragged_shapes(w_dtype, x_dtype, flags):
+    # several row tiles per expert, a ragged last tile, f != f_s, d not a power of two
+    inp = moe_synth.make_custom(T=301, d=384, E=16, k=4, f=192, fs=128, x_dtype=x_dtype, w_dtype=w_dtype, seed=21)
+    _, _, y, ids, w, offs = run_layer(inp, flags)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 1), (5, 8, 8), (40, 1, 1), (17, 256, 16), (3, 128, 6)])
+def test_edge_shapes(T, E, k):
+    inp = moe_synth.make_custom(T=T, d=256, E=E, k=k, f=64, fs=64, x_dtype="bf16", w_dtype="e4m3", seed=T + E)
+    _, _, y, ids, w, offs = run_layer(inp)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids)
+    if k == 1:
+        assert np.all(w == 1.0)
+
+
+def test_skew_has_empty_and_hot_experts():
+    inp = workload("skew")
+    _, _, _, ids, _, offs = run_layer(inp)
+    counts = np.diff(offs)
+    assert (counts == 0).sum() >= 4
+    assert counts.max() / counts.mean() > 7.5
+
+
+def test_bf16_output():
+    inp = workload("decode")
+    _, _, y, ids, _, _ = run_layer(inp, y_dtype=abi.MOE_BF16)
+    check_output(inp, y, ids)
+
+
+def test_zero_tokens():
+    inp = moe_synth.make_custom(T=4, d=128, E=8, k=2, f=64, fs=64, x_dtype="bf16", w_dtype="e4m3")
+    layer = MoELayer(inp)
+    x = device_x(inp)[:0]
+    y = layer.forward(x)
+    assert y.shape == (0, 128)
+    assert abi.moe_get_device_status() == 0
+
+
+def test_deterministic_bitwise():
+    inp = workload("decode")
+    layer = MoELayer(inp)
+    x = device_x(inp)
+    y1 = layer.forward(x).clone()
+    y2 = layer.forward(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_stepwise_calls_match_layer_forward():
+    inp = moe_synth.make_custom(T=96, d=256, E=32, k=6, f=128, fs=64, x_dtype="bf16", w_dtype="e4m3", seed=5)
+    layer = MoELayer(inp)
+    x = device_x(inp)
+    y_full = layer.forward(x)
+    cfg = layer.config()
+    T, k, E, d = inp.cfg.T, inp.cfg.k, inp.cfg.E, inp.cfg.d
+    dev = "cuda"
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(T * k, dtype=torch.int32, device=dev)
+    row_of = torch.empty(T * k, dtype=torch.int32, device=dev)
+    out_perm = torch.empty((T * k, d), dtype=torch.float32, device=dev)
+    shared = torch.empty((T, d), dtype=torch.float32, device=dev)
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    ws = layer.workspace()
+    abi.moe_route(cfg, x, layer.w_router, layer.bias, ids, w)
+    abi.moe_permute(cfg, ids, offs, sp, row_of, ws)
+    abi.moe_expert_ffn(cfg, x, w, offs, sp, layer.weights, out_perm, shared, ws)
+    abi.moe_combine(cfg, out_perm, row_of, shared, y)
+    assert abi.moe_get_device_status() == 0
+    assert torch.equal(y, y_full)
+    # permutation: bit-exact against the oracle's on the same ids
+    c_ref, o_ref, sp_ref, r_ref = oracle.permute(ids.cpu().numpy(), E)
+    assert np.array_equal(offs.cpu().numpy(), o_ref)
+    assert np.array_equal(sp.cpu().numpy(), sp_ref)
+    assert np.array_equal(row_of.cpu().numpy(), r_ref)
+    # out_perm rows and the shared output, element by element
+    ref = oracle.layer_forward(inp)
+    ids_np = ids.cpu().numpy()
+    assert np.array_equal(ids_np, ref["ids"])
+    for name, got, want in (("out_perm", out_perm, ref["out_perm"]), ("shared", shared, ref["shared"])):
+        g = got.cpu().numpy().astype(np.float64)
+        rel = np.linalg.norm(g - want) / np.linalg.norm(want)
+        assert rel < 5e-3, (name, rel)
+
+
+@pytest.mark.parametrize("P_mult", [1, 7])
+def test_permute_bit_exact_large(P_mult):
+    # many chunks of the counting sort; random ids with empty experts
+    E, k = 128, 6
+    T = 2048 * P_mult + 5
+    rng = np.random.default_rng(P_mult)
+    ids = np.stack([rng.choice(E - 3, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    cfg = abi.make_config(T, 128, E, k, 64, 64)
+    dev = "cuda"
+    ids_d = torch.from_numpy(ids).to(dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(T * k, dtype=torch.int32, device=dev)
+    row_of = torch.empty(T * k, dtype=torch.int32, device=dev)
+    ws = torch.empty(abi.moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    abi.moe_permute(cfg, ids_d, offs, sp, row_of, ws)
+    assert abi.moe_get_device_status() == 0
+    c_ref, o_ref, sp_ref, r_ref = oracle.permute(ids, E)
+    assert np.array_equal(offs.cpu().numpy(), o_ref)
+    assert np.array_equal(sp.cpu().numpy(), sp_ref)
+    assert np.array_equal(row_of.cpu().numpy(), r_ref)
+
+
+def test_out_of_range_ids_reported_not_faulted():
+    E, k, T = 16, 2, 100
+    ids = np.tile(np.array([[0, 1]], dtype=np.int32), (T, 1))
+    ids[7, 1] = 99          # corrupt
+    ids[50, 0] = -3
+    cfg = abi.make_config(T, 128, E, k, 64, 64)
+    dev = "cuda"
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sp = torch.zeros(T * k, dtype=torch.int32, device=dev)
+    row_of = torch.zeros(T * k, dtype=torch.int32, device=dev)
+    ws = torch.empty(abi.moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    abi.moe_permute(cfg, torch.from_numpy(ids).to(dev), offs, sp, row_of, ws)
+    assert abi.moe_get_device_status() == 6     # MOE_ERR_DEVICE_BOUNDS
+    assert offs.cpu().numpy()[-1] == T * k - 2
+    assert abi.moe_get_device_status() == 0     # cleared
+
+
+def test_router_alone_with_bias():
+    inp = moe_synth.make_custom(T=77, d=512, E=64, k=5, f=64, fs=64, x_dtype="bf16", w_dtype="e4m3", seed=9)
+    inp.bias = np.linspace(-2, 2, 64).astype(np.float32)
+    layer = MoELayer(inp)
+    cfg = layer.config()
+    ids = torch.empty((77, 5), dtype=torch.int32, device="cuda")
+    w = torch.empty((77, 5), dtype=torch.float32, device="cuda")
+    abi.moe_route(cfg, device_x(inp), layer.w_router, layer.bias, ids, w)
+    assert abi.moe_get_device_status() == 0
+    ids_np, w_np = ids.cpu().numpy(), w.cpu().numpy()
+    _, o = check_routing(inp, ids_np, w_np, oracle.permute(ids_np, 64)[1])
+
+
+# Shapes whose average rows per expert select each tensor-core token tile
+# (TN = 8, 16, 32, 64, 128) with ragged last tiles, f != f_s, and a d that is
+# not a power of two.
+TC_SHAPES = [
+    dict(T=20, d=384, E=32, k=2, f=256, fs=128),     # ~1 row / expert   -> TN 8
+    dict(T=64, d=256, E=16, k=2, f=128, fs=256),     # 8 rows / expert   -> TN 16
+    dict(T=100, d=384, E=16, k=2, f=256, fs=128),    # 12.5              -> TN 32
+    dict(T=160, d=256, E=16, k=4, f=128, fs=128),    # 40                -> TN 64
+    dict(T=301, d=384, E=16, k=4, f=256, fs=384),    # 75                -> TN 128
+]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=[f"T{s['T']}_E{s['E']}" for s in TC_SHAPES])
+def test_tensor_core_path_tiles(shape):
+    inp = moe_synth.make_custom(x_dtype="bf16", w_dtype="e4m3", seed=shape["T"], **shape)
+    _, _, y, ids, w, offs = run_layer(inp)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids)
+
+
+def test_tensor_core_matches_simt_closely():
+    # both paths against each other on the decode workload: the two-term FP8
+    # activation split keeps the tensor-core result within bf16-rounding
+    # distance of the fp32 CUDA-core result
+    inp = workload("decode")
+    _, _, y_tc, ids_tc, _, _ = run_layer(inp, 0)
+    _, _, y_s, ids_s, _, _ = run_layer(inp, abi.MOE_FLAG_SIMT_FFN)
+    assert np.array_equal(ids_tc, ids_s)
+    rel = np.linalg.norm(y_tc - y_s) / np.linalg.norm(y_s)
+    assert rel < 3e-3, rel

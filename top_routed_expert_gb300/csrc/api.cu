@@ -1,0 +1,311 @@
+// Host side of the C ABI declared in include/moe_gb300.h: argument
+// validation, workspace planning and launch sequencing on the caller's
+// stream.  No call synchronises the host or allocates device memory.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+// launchers (one per translation unit)
+cudaError_t launch_router(const void* x, bool x_bf16, const float* wr, const float* bias, int T, int d, int E,
+                          int k, int32_t* ids, float* w, unsigned* status, int num_sms, cudaStream_t stream);
+size_t permute_ws_bytes(int P, int E);
+cudaError_t launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, int32_t* sorted_pair,
+                           int32_t* row_of, void* ws, unsigned* status, cudaStream_t stream);
+size_t ffn_simt_ws_bytes(int T, int k, int f, int fs);
+cudaError_t launch_ffn_simt(const void* x, bool x_bf16, int w_dtype, const float* topk_w, const int32_t* offsets,
+                            const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                            int T, int d, int E, int k, int f, int fs, void* ws, unsigned* status,
+                            cudaStream_t stream);
+bool ffn_tc_supported(const moe_config_t& c);
+size_t ffn_tc_ws_bytes(const moe_config_t& c);
+cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
+                          const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                          void* ws, unsigned* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_combine(const float* out_perm, const int32_t* row_of, const float* shared, void* y,
+                           bool y_bf16, int T, int d, int k, unsigned* status, int num_sms, cudaStream_t stream);
+}  // namespace moe
+
+// Per-device status word (see moe_get_device_status).
+__device__ unsigned g_moe_status;
+
+namespace moe {
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+}  // namespace moe
+
+namespace {
+
+using namespace moe;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool arch_ok = false;
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Looks up (once per device) the SM count, the architecture and the status
+// word address of the current device.
+moe_status_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    di.arch_ok = (major == 10 && minor == 3);
+    di.num_sms = sms;
+    if (di.arch_ok) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_moe_status) != cudaSuccess) return MOE_ERR_CUDA;
+      di.status = static_cast<unsigned*>(p);
+    }
+    di.ready = true;
+  }
+  *out = di;
+  return di.arch_ok ? MOE_OK : MOE_ERR_ARCH;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status_t validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d_model <= 0 || c->d_model % 128 != 0 || c->d_model > 16384) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts < 1 || c->n_experts > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->d_ff <= 0 || c->d_ff % 64 != 0 || c->d_ff_shared <= 0 || c->d_ff_shared % 64 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->d_ff > 65536 || c->d_ff_shared > 65536) return MOE_ERR_INVALID_ARG;
+  if (c->x_dtype != MOE_F32 && c->x_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_E4M3 && c->w_dtype != MOE_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (c->y_dtype != MOE_F32 && c->y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(c->T) * c->top_k > (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~MOE_FLAG_SIMT_FFN) != 0) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+bool use_tc(const moe_config_t& c) {
+  return !(c.flags & MOE_FLAG_SIMT_FFN) && ffn_tc_supported(c);
+}
+
+size_t ffn_ws_bytes(const moe_config_t& c) {
+  size_t s = ffn_simt_ws_bytes(c.T, c.top_k, c.d_ff, c.d_ff_shared);
+  if (use_tc(c)) s = std::max(s, ffn_tc_ws_bytes(c));
+  return s;
+}
+
+// Workspace layout of moe_layer_forward.
+struct FwdPlan {
+  size_t ids, w, offsets, sorted_pair, row_of, out_perm, shared_out, scratch, total;
+};
+
+FwdPlan plan_forward(const moe_config_t& c) {
+  const size_t P = static_cast<size_t>(c.T) * c.top_k;
+  FwdPlan p;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes, 256); return at; };
+  p.ids = take(sizeof(int32_t) * P);
+  p.w = take(sizeof(float) * P);
+  p.offsets = take(sizeof(int32_t) * (c.n_experts + 1));
+  p.sorted_pair = take(sizeof(int32_t) * P);
+  p.row_of = take(sizeof(int32_t) * P);
+  p.out_perm = take(sizeof(float) * P * c.d_model);
+  p.shared_out = take(sizeof(float) * static_cast<size_t>(c.T) * c.d_model);
+  p.scratch = take(std::max(permute_ws_bytes(static_cast<int>(P), c.n_experts), ffn_ws_bytes(c)));
+  p.total = o;
+  return p;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool weights_ok(const moe_config_t& c, const moe_weights_t* w) {
+  if (!w || !w->w13 || !w->w2 || !w->s13 || !w->s2) return false;
+  const void* q[4] = {w->w13, w->w2, w->s13, w->s2};
+  for (const void* p : q)
+    if (!aligned(p, 16)) return false;
+  if (c.w_dtype == MOE_E4M3 || c.w_dtype == MOE_NVFP4) {
+    const void* s[4] = {w->w13_scale, w->w2_scale, w->s13_scale, w->s2_scale};
+    for (const void* p : s)
+      if (!p || !aligned(p, 4)) return false;
+  }
+  if (c.w_dtype == MOE_NVFP4) {
+    if (!w->w13_gscale || !w->w2_gscale || !w->s13_gscale || !w->s2_gscale) return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_str(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+    case MOE_ERR_ARCH: return "MOE_ERR_ARCH";
+    case MOE_ERR_DEVICE_NONFINITE: return "MOE_ERR_DEVICE_NONFINITE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+size_t moe_workspace_bytes(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  return plan_forward(*cfg).total;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const float* w_router, const float* expert_bias,
+                       int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !w_router || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) ||
+      (expert_bias && !aligned(expert_bias, 4)))
+    return MOE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_router(x, cfg->x_dtype == MOE_BF16, w_router, expert_bias, cfg->T, cfg->d_model,
+                                   cfg->n_experts, cfg->top_k, topk_ids, topk_w, di.status, di.num_sms,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32_t* expert_offsets,
+                         int32_t* sorted_pair, int32_t* row_of, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!expert_offsets) return MOE_ERR_INVALID_ARG;
+  const int P = cfg->T * cfg->top_k;
+  if (P > 0 && (!topk_ids || !sorted_pair || !row_of)) return MOE_ERR_INVALID_ARG;
+  const size_t need = permute_ws_bytes(P, cfg->n_experts);
+  if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_permute(topk_ids, P, cfg->n_experts, expert_offsets, sorted_pair, row_of, ws,
+                                    di.status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float* topk_w,
+                            const int32_t* expert_offsets, const int32_t* sorted_pair, const moe_weights_t* weights,
+                            float* out_perm, float* shared_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !topk_w || !expert_offsets || !sorted_pair || !out_perm || !shared_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out_perm, 16) || !aligned(shared_out, 16)) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(*cfg, weights)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < ffn_ws_bytes(*cfg)) return MOE_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use_tc(*cfg))
+    return cuda_status(launch_ffn_tc(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
+                                     ws, di.status, di.num_sms, s));
+  return cuda_status(launch_ffn_simt(x, cfg->x_dtype == MOE_BF16, cfg->w_dtype, topk_w, expert_offsets,
+                                     sorted_pair, weights, out_perm, shared_out, cfg->T, cfg->d_model,
+                                     cfg->n_experts, cfg->top_k, cfg->d_ff, cfg->d_ff_shared, ws, di.status, s));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const int32_t* row_of,
+                         const float* shared_out, void* y, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!out_perm || !row_of || !shared_out || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(out_perm, 16) || !aligned(shared_out, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_combine(out_perm, row_of, shared_out, y, cfg->y_dtype == MOE_BF16, cfg->T,
+                                    cfg->d_model, cfg->top_k, di.status, di.num_sms,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const float* w_router,
+                               const float* expert_bias, const moe_weights_t* weights, void* y,
+                               int32_t* topk_ids_opt, float* topk_w_opt, int32_t* expert_offsets_opt, void* ws,
+                               size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) {
+    if (expert_offsets_opt) {
+      DeviceInfo di;
+      if ((st = device_info(&di)) != MOE_OK) return st;
+      return cuda_status(cudaMemsetAsync(expert_offsets_opt, 0, sizeof(int32_t) * (cfg->n_experts + 1),
+                                         static_cast<cudaStream_t>(stream)));
+    }
+    return MOE_OK;
+  }
+  if (!x || !w_router || !y) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(*cfg, weights)) return MOE_ERR_INVALID_ARG;
+  const FwdPlan p = plan_forward(*cfg);
+  if (!ws || ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  char* base = static_cast<char*>(ws);
+  int32_t* ids = reinterpret_cast<int32_t*>(base + p.ids);
+  float* w = reinterpret_cast<float*>(base + p.w);
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + p.offsets);
+  int32_t* sorted_pair = reinterpret_cast<int32_t*>(base + p.sorted_pair);
+  int32_t* row_of = reinterpret_cast<int32_t*>(base + p.row_of);
+  float* out_perm = reinterpret_cast<float*>(base + p.out_perm);
+  float* shared_out = reinterpret_cast<float*>(base + p.shared_out);
+  void* scratch = base + p.scratch;
+  const size_t scratch_bytes = p.total - p.scratch;
+  if ((st = moe_route(cfg, x, w_router, expert_bias, ids, w, stream)) != MOE_OK) return st;
+  if ((st = moe_permute(cfg, ids, offsets, sorted_pair, row_of, scratch, scratch_bytes, stream)) != MOE_OK)
+    return st;
+  if ((st = moe_expert_ffn(cfg, x, w, offsets, sorted_pair, weights, out_perm, shared_out, scratch, scratch_bytes,
+                           stream)) != MOE_OK)
+    return st;
+  if ((st = moe_combine(cfg, out_perm, row_of, shared_out, y, stream)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t P = static_cast<size_t>(cfg->T) * cfg->top_k;
+  if (topk_ids_opt &&
+      cudaMemcpyAsync(topk_ids_opt, ids, sizeof(int32_t) * P, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (topk_w_opt && cudaMemcpyAsync(topk_w_opt, w, sizeof(float) * P, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (expert_offsets_opt &&
+      cudaMemcpyAsync(expert_offsets_opt, offsets, sizeof(int32_t) * (cfg->n_experts + 1),
+                      cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }
+
+moe_status_t moe_get_device_status(moe_stream_t stream) {
+  DeviceInfo di;
+  moe_status_t st = device_info(&di);
+  if (st != MOE_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, di.status, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(di.status, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return static_cast<moe_status_t>(v);
+}
+
+}  // extern "C"

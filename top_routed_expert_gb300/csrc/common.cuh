@@ -1,0 +1,87 @@
+// Shared device helpers of the MoE layer kernels (sm_103a).
+#pragma once
+
+#include <algorithm>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+
+// Host-side count of kernel launches (moe_launch_count); defined in api.cu.
+void count_launches(int n);
+constexpr int kMaxGroups = kMaxExperts + 1;   // routed experts + the shared expert
+
+// Device status word: kernels record the first fault they see with
+// atomicCAS(0 -> code) and carry on with the fault contained (skip the bad
+// access, return from a wait).  The host reads and clears it.
+__device__ __forceinline__ void set_status(unsigned* status, unsigned code) {
+  if (status) atomicCAS(status, 0u, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Activation element -> float (x is fp32 or bf16).
+template <typename XT> __device__ __forceinline__ float x_to_float(XT v);
+template <> __device__ __forceinline__ float x_to_float<float>(float v) { return v; }
+template <> __device__ __forceinline__ float x_to_float<uint16_t>(uint16_t v) { return bf16_bits_to_float(v); }
+
+// FP8 E4M3 code -> float, through the hardware conversion.
+__device__ __forceinline__ float e4m3_to_float(uint8_t code) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// E2M1 code (low 4 bits) -> float.  Magnitudes by code 0..7 are the format's
+// eight values 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 is the sign.
+__device__ __forceinline__ float e2m1_to_float(uint32_t code) {
+  const uint32_t e = (code >> 1) & 3u, m = code & 1u;
+  float mag = (e == 0) ? 0.5f * static_cast<float>(m)
+                       : (1.0f + 0.5f * static_cast<float>(m)) * static_cast<float>(1u << (e - 1));
+  return (code & 8u) ? -mag : mag;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Device-side group table: routed experts 0..E-1 plus the shared expert as
+// group E.  rows(g) = routed count or T; tiles(g) = ceil(rows/TM).
+// Fills tile_start[0..E+1] (exclusive prefix of tiles) in shared memory with
+// one block-wide pass.
+__device__ __forceinline__ void build_tile_table(const int32_t* __restrict__ offsets, int E, int T, int TM,
+                                                 int* s_tile_start, int* s_scratch) {
+  const int G = E + 1;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    int rows = (g < E) ? (offsets[g + 1] - offsets[g]) : T;
+    s_scratch[g] = (max(rows, 0) + TM - 1) / TM;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int g = 0; g < G; ++g) { s_tile_start[g] = acc; acc += s_scratch[g]; }
+    s_tile_start[G] = acc;
+  }
+  __syncthreads();
+}
+
+// Largest g with tile_start[g] <= i (tile_start non-decreasing, G+1 entries).
+__device__ __forceinline__ int find_group(const int* s_tile_start, int G, int i) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (s_tile_start[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace moe

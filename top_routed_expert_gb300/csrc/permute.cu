@@ -1,0 +1,132 @@
+// Token permutation into per-expert groups: the grouping that feeds the
+// grouped expert GEMMs (Sarvam blog, H100 baseline section: expert
+// parallelism "uses grouped GEMM kernels"; Table 1 row "Routed expert
+// compute").
+//
+// A stable counting sort of the T*k pairs p = t*k+j keyed by expert:
+//   1. hist    : each CTA counts the experts of its chunk of pairs.
+//   2. scan    : one CTA turns the per-chunk counts into expert offsets and a
+//                per-(chunk, expert) base position.
+//   3. scatter : each CTA walks its chunk in pair order and places every pair
+//                at base + (pairs of the same expert before it in the chunk),
+//                found with a warp match and a per-warp count table.
+// Deterministic and stable: within an expert the pairs come out in ascending
+// p, hence ascending token.  Ids outside [0, E) are skipped and recorded in
+// the device status word.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kPermThreads = 256;
+constexpr int kPermChunk = 2048;          // pairs per CTA
+constexpr int kPermMaxE = 256;
+
+__global__ void __launch_bounds__(kPermThreads)
+permute_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ blk_counts,
+                    unsigned* status) {
+  __shared__ int hist[kPermMaxE];
+  for (int e = threadIdx.x; e < E; e += kPermThreads) hist[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kPermChunk;
+  const int end = min(P, base + kPermChunk);
+  for (int p = base + threadIdx.x; p < end; p += kPermThreads) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else set_status(status, MOE_ERR_DEVICE_BOUNDS);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kPermThreads) blk_counts[blockIdx.x * E + e] = hist[e];
+}
+
+// One CTA of kPermThreads >= E threads.
+__global__ void __launch_bounds__(kPermThreads)
+permute_scan_kernel(const int32_t* __restrict__ blk_counts, int nblk, int E, int P,
+                    int32_t* __restrict__ offsets, int32_t* __restrict__ blk_base) {
+  __shared__ int tot[kPermMaxE];
+  __shared__ int off[kPermMaxE + 1];
+  const int e = threadIdx.x;
+  if (e < E) {
+    int s = 0;
+    for (int b = 0; b < nblk; ++b) s += blk_counts[b * E + e];
+    tot[e] = s;
+  }
+  __syncthreads();
+  if (e == 0) {
+    int acc = 0;
+    for (int i = 0; i < E; ++i) { off[i] = acc; acc += tot[i]; }
+    off[E] = acc;
+  }
+  __syncthreads();
+  if (e < E) {
+    offsets[e] = off[e];
+    int run = off[e];
+    for (int b = 0; b < nblk; ++b) {
+      blk_base[b * E + e] = run;
+      run += blk_counts[b * E + e];
+    }
+  }
+  if (e == 0) offsets[E] = off[E];
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+permute_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* __restrict__ blk_base,
+                       int32_t* __restrict__ sorted_pair, int32_t* __restrict__ row_of) {
+  constexpr int W = kPermThreads / 32;
+  __shared__ int run[kPermMaxE];        // next free position per expert for this CTA
+  __shared__ int wcnt[W][kPermMaxE];    // pairs per (warp, expert) in the current sub-chunk
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < E; e += kPermThreads) run[e] = blk_base[blockIdx.x * E + e];
+  const int base = blockIdx.x * kPermChunk;
+  const int end = min(P, base + kPermChunk);
+  for (int c0 = base; c0 < end; c0 += kPermThreads) {
+    for (int i = tid; i < W * E; i += kPermThreads) wcnt[i / E][i % E] = 0;
+    __syncthreads();
+    const int p = c0 + tid;
+    int e = -1;
+    if (p < end) {
+      e = ids[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const unsigned lt = (1u << lane) - 1u;
+    const int rank_in_warp = __popc(same & lt);
+    if (e >= 0 && rank_in_warp == 0) wcnt[warp][e] = __popc(same);
+    __syncthreads();
+    if (e >= 0) {
+      int pos = run[e] + rank_in_warp;
+      for (int w2 = 0; w2 < warp; ++w2) pos += wcnt[w2][e];
+      sorted_pair[pos] = p;
+      row_of[p] = pos;
+    }
+    __syncthreads();
+    for (int i = tid; i < E; i += kPermThreads) {
+      int s = 0;
+      for (int w2 = 0; w2 < W; ++w2) s += wcnt[w2][i];
+      run[i] += s;
+    }
+    __syncthreads();
+  }
+}
+
+size_t permute_ws_bytes(int P, int E) {
+  const int nblk = ceil_div(P, kPermChunk);
+  return 2 * align_up(sizeof(int32_t) * static_cast<size_t>(nblk) * E, 256);
+}
+
+cudaError_t launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, int32_t* sorted_pair,
+                           int32_t* row_of, void* ws, unsigned* status, cudaStream_t stream) {
+  const int nblk = ceil_div(P, kPermChunk);
+  int32_t* blk_counts = static_cast<int32_t*>(ws);
+  int32_t* blk_base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
+                                                 align_up(sizeof(int32_t) * static_cast<size_t>(nblk) * E, 256));
+  if (P == 0) {
+    return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), stream);
+  }
+  count_launches(3);
+  permute_hist_kernel<<<nblk, kPermThreads, 0, stream>>>(ids, P, E, blk_counts, status);
+  permute_scan_kernel<<<1, kPermThreads, 0, stream>>>(blk_counts, nblk, E, P, offsets, blk_base);
+  permute_scatter_kernel<<<nblk, kPermThreads, 0, stream>>>(ids, P, E, blk_base, sorted_pair, row_of);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
