@@ -1,13 +1,560 @@
-// Tensor-core (tcgen05) grouped expert FFN -- placeholder until implemented.
+// Grouped SwiGLU expert FFN on the 5th-generation tensor cores (tcgen05,
+// TMEM accumulators, TMA-fed shared memory) for FP8 E4M3 expert weights.
+// Sarvam blog, Table 1 rows "Routed expert compute" / "Shared expert
+// compute"; Sarvam summary section 2.1 (FP8 expert weights, one byte per
+// parameter); H100 baseline section (grouped GEMM kernels over the experts).
+//
+// Design (GB300-first, not the pages' H100 kernels):
+//  * swap-AB: the weight rows fill the MMA's M = 128 lanes (A operand, read
+//    straight from HBM by TMA as raw E4M3 codes), the routed tokens of a
+//    group are the N columns (B operand).  Decode groups hold ~3 tokens, so
+//    the tile stays full and the kernel streams weights at HBM speed.
+//  * activations enter the FP8 MMA as two E4M3 terms with a per-row power-
+//    of-two scale s:  v = s * (hi + lo/16).  For a bf16 input this split is
+//    exact apart from elements below 2^-6 s (absolute error < 2^-14 s), so
+//    the product equals the bf16-activation product; hi and lo are adjacent
+//    N columns and the epilogue adds them.  Per-channel weight scales and the
+//    row scale are applied in the epilogue.
+//  * gemm1 (gate+up, two accumulators) -> silu(g)*u -> H (bf16);
+//    H is re-split into two E4M3 terms per row; gemm2 (down) applies the gate
+//    weight and writes out_perm (routed) / shared_out (shared expert).
+//  * the shared expert is group E of the same launches (rows = all tokens).
+//  * persistent CTAs walk a device-built tile list (group, weight tile,
+//    token tile) -- no host read-back of the expert counts.
+//  * warp roles: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
+//    warps 2-5 = epilogue.  Every mbarrier wait is bounded; on expiry the
+//    kernel records MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs,
+//    frees TMEM and returns.
+#include <cuda.h>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
-bool ffn_tc_supported(const moe_config_t&) { return false; }
-size_t ffn_tc_ws_bytes(const moe_config_t&) { return 0; }
-cudaError_t launch_ffn_tc(const moe_config_t&, const void*, const float*, const int32_t*, const int32_t*,
-                          const moe_weights_t*, float*, float*, void*, unsigned*, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+using namespace ptx;
+
+constexpr int kTcThreads = 192;
+constexpr int kBK = 128;                // K bytes (= FP8 elements) per pipeline stage
+constexpr int kBM = 128;                // weight rows per tile = MMA M
+constexpr int kMaxStages = 8;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: no legitimate wait comes close
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
+constexpr uint32_t kABytes = kBM * kBK;            // 16 KB per weight tile
+constexpr int kSmemBudget = 220 * 1024;
+
+struct TcArgs {
+  const int32_t* offsets;      // [E+1]
+  const int32_t* sorted_pair;  // [P]
+  const float* topk_w;         // [P]
+  const float* a_scale;        // routed per-output-row weight scales: w13_scale [E][2f] | w2_scale [E][d]
+  const float* as_scale;       // shared: s13_scale [2fs] | s2_scale [d]
+  const float* b_scale;        // per-row activation scale [P+T]
+  __nv_bfloat16* h;            // gemm1 out: H [(P+T)][fmax]
+  float* out_perm;             // gemm2 out: [P][d]
+  float* shared_out;           // gemm2 out: [T][d]
+  int T, k, E, P, d, f, fs, fmax;
+  int TN;                      // token rows per tile; MMA N = 2*TN
+  int stages, acc_bufs, tmem_cols;
+  unsigned* status;
+};
+
+struct GroupTable {
+  int tile_start[kMaxGroups + 1];
+  int row_base[kMaxGroups];    // first row of the group in the (P+T)-row activation space
+  int rows[kMaxGroups];
+  int mtiles[kMaxGroups];
+};
+
+struct __align__(16) TcCtrl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  GroupTable gt;
+};
+
+struct Tile {
+  int g, wt, row0, nrows;
+};
+
+__device__ __forceinline__ Tile decode_tile(const GroupTable& gt, int G, int i, int TN) {
+  Tile t;
+  t.g = find_group(gt.tile_start, G, i);
+  const int local = i - gt.tile_start[t.g];
+  const int mt_n = gt.mtiles[t.g];
+  t.wt = local / mt_n;
+  const int mt = local - t.wt * mt_n;
+  t.row0 = gt.row_base[t.g] + mt * TN;
+  t.nrows = min(TN, gt.rows[t.g] - mt * TN);
+  return t;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAS,
+              const __grid_constant__ CUtensorMap mapB, TcArgs a) {
+  constexpr int NA = (MODE == 1) ? 2 : 1;   // weight tiles per stage (gate + up, or down)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int N = 2 * a.TN;
+  const uint32_t b_bytes = static_cast<uint32_t>(N) * kBK;
+  const uint32_t stage_bytes = NA * kABytes + ((b_bytes + 1023u) & ~1023u);
+  TcCtrl* c = reinterpret_cast<TcCtrl*>(smem + a.stages * stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.E + 1;
+  volatile int* abort = &c->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_u32(&c->full[s]), 1);
+      mbar_init(smem_u32(&c->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&c->tfull[b]), 1);
+      mbar_init(smem_u32(&c->tempty[b]), 128);
+    }
+    mbar_init(smem_u32(&c->drain), 1);
+    c->abort = 0;
+    fence_barrier_init();
+    // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
+    int acc = 0;
+    for (int g = 0; g < G; ++g) {
+      int base, rows;
+      if (g < a.E) {
+        base = a.offsets[g];
+        rows = a.offsets[g + 1] - base;
+        if (base < 0 || rows < 0 || base + rows > a.P) {
+          set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+          base = 0;
+          rows = 0;
+        }
+      } else {
+        base = a.P;
+        rows = a.T;
+      }
+      const int wt = (MODE == 1) ? ((g < a.E ? a.f : a.fs) / kBM) : (a.d / kBM);
+      const int mt = (rows + a.TN - 1) / a.TN;
+      c->gt.tile_start[g] = acc;
+      c->gt.row_base[g] = base;
+      c->gt.rows[g] = rows;
+      c->gt.mtiles[g] = mt;
+      acc += mt * wt;
+    }
+    c->gt.tile_start[G] = acc;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapAS);
+    tma_prefetch_desc(&mapB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c->tmem_base;
+  const int total = c->gt.tile_start[G];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int st = 0;
+      uint32_t ph = 0, pending = 0, last_par = 0;
+      for (int i = blockIdx.x; i < total && !*abort; i += gridDim.x) {
+        const Tile t = decode_tile(c->gt, G, i, a.TN);
+        const bool shr = t.g == a.E;
+        const CUtensorMap* mA = shr ? &mapAS : &mapA;
+        int arow0, arow1 = 0, K;
+        if (MODE == 1) {
+          const int width = shr ? a.fs : a.f;
+          const int base = shr ? 0 : t.g * 2 * a.f;
+          arow0 = base + t.wt * kBM;
+          arow1 = base + width + t.wt * kBM;
+          K = a.d;
+        } else {
+          arow0 = (shr ? 0 : t.g * a.d) + t.wt * kBM;
+          K = shr ? a.fs : a.f;
+        }
+        const int brow = 2 * t.row0;
+        for (int kb = 0; kb < K / kBK; ++kb) {
+          if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, kWaitLimitNs)) break;
+          const uint32_t full = smem_u32(&c->full[st]);
+          mbar_arrive_expect_tx(full, NA * kABytes + b_bytes);
+          const uint32_t sA = smem_u32(smem + st * stage_bytes);
+          tma_load_2d(sA, mA, kb * kBK, arow0, full);
+          if (MODE == 1) tma_load_2d(sA + kABytes, mA, kb * kBK, arow1, full);
+          tma_load_2d(sA + NA * kABytes, &mapB, kb * kBK, brow, full);
+          pending |= 1u << st;
+          last_par = (last_par & ~(1u << st)) | (ph << st);
+          if (++st == a.stages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // every issued copy must land before the CTA may exit
+      int no_abort = 0;
+      for (int s = 0; s < a.stages; ++s)
+        if (pending & (1u << s)) mbar_wait(smem_u32(&c->full[s]), (last_par >> s) & 1u, &no_abort, kDrainLimitNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_f8_e4m3(kBM, N);
+      int st = 0, ab = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+        const Tile t = decode_tile(c->gt, G, i, a.TN);
+        const bool shr = t.g == a.E;
+        const int K = (MODE == 1) ? a.d : (shr ? a.fs : a.f);
+        if (!mbar_wait(smem_u32(&c->tempty[ab]), aph ^ 1u, abort, kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem + static_cast<uint32_t>(ab * NA * N);
+        const uint32_t d1 = d0 + static_cast<uint32_t>(N);
+        for (int kb = 0; kb < K / kBK; ++kb) {
+          if (!mbar_wait(smem_u32(&c->full[st]), ph, abort, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + st * stage_bytes);
+          const uint64_t da0 = desc_sw128(sA);
+          const uint64_t da1 = desc_sw128(sA + kABytes);
+          const uint64_t db = desc_sw128(sA + NA * kABytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk) {
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            mma_f8f6f4(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
+            if (MODE == 1) mma_f8f6f4(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+          }
+          mma_commit(smem_u32(&c->empty[st]));
+          if (++st == a.stages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&c->tfull[ab]));
+        if (++ab == a.acc_bufs) {
+          ab = 0;
+          aph ^= 1u;
+        }
+      }
+      // no MMA may still be running when TMEM is released
+      mma_commit(smem_u32(&c->drain));
+      int no_abort = 0;
+      mbar_wait(smem_u32(&c->drain), 0, &no_abort, kDrainLimitNs);
+    }
+  } else {
+    // -------------------------------------------------- epilogue (warps 2..5)
+    const int sub = warp & 3;                       // TMEM lanes this warp may access
+    const int n = sub * 32 + lane;                  // weight row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
+    int ab = 0;
+    uint32_t aph = 0;
+    for (int i = blockIdx.x; i < total; i += gridDim.x) {
+      const Tile t = decode_tile(c->gt, G, i, a.TN);
+      const bool shr = t.g == a.E;
+      if (!mbar_wait(smem_u32(&c->tfull[ab]), aph, abort, kWaitLimitNs)) break;
+      tc_fence_after();
+      if (MODE == 1) {
+        const int width = shr ? a.fs : a.f;
+        const int col = t.wt * kBM + n;
+        const float sg = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + col];
+        const float su = shr ? a.as_scale[width + col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + a.f + col];
+        const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float gv[16], uv[16];
+          tmem_ld16(cb + c0, gv);
+          tmem_ld16(cb + N + c0, uv);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = c0 / 2 + jj;
+            if (j < t.nrows) {
+              const int row = t.row0 + j;
+              const float sx = a.b_scale[row];
+              const float g = (gv[2 * jj] + gv[2 * jj + 1] * 0.0625f) * sx * sg;
+              const float u = (uv[2 * jj] + uv[2 * jj + 1] * 0.0625f) * sx * su;
+              a.h[static_cast<size_t>(row) * a.fmax + col] = __float2bfloat16_rn(silu(g) * u);
+            }
+          }
+        }
+      } else {
+        const int col = t.wt * kBM + n;
+        const float sw = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * a.d + col];
+        const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float dv[16];
+          tmem_ld16(cb + c0, dv);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = c0 / 2 + jj;
+            if (j < t.nrows) {
+              const int row = t.row0 + j;
+              const float o = (dv[2 * jj] + dv[2 * jj + 1] * 0.0625f) * a.b_scale[row] * sw;
+              if (shr) {
+                a.shared_out[static_cast<size_t>(row - a.P) * a.d + col] = o;
+              } else {
+                const int p = a.sorted_pair[row];
+                float gw = 0.f;
+                if (p >= 0 && p < a.P) gw = a.topk_w[p];
+                else if (lane == 0) set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+                a.out_perm[static_cast<size_t>(row) * a.d + col] = o * gw;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&c->tempty[ab]));
+      if (++ab == a.acc_bufs) {
+        ab = 0;
+        aph ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+  if (threadIdx.x == 0 && c->abort) set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// Row quantiser: v = s * (hi + lo/16), s = 2^ceil(log2(amax/448)), hi and lo
+// E4M3 (round to nearest even, saturating).  One warp per row of the
+// (P+T)-row activation space.  GATHER_X: row r < P takes x[sorted_pair[r]/k],
+// row P+t takes x[t] (width d); otherwise row r of H (width f for routed
+// rows, f_s for shared rows).  Output q[2r] = hi codes, q[2r+1] = lo codes.
+template <bool GATHER_X>
+__global__ void __launch_bounds__(256)
+quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
+                   int width_r, int width_s, int src_stride, uint8_t* __restrict__ q, int q_stride,
+                   float* __restrict__ scale, unsigned* status) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= P + T) return;
+  const uint16_t* s;
+  int width;
+  uint8_t* qh = q + static_cast<size_t>(2 * row) * q_stride;
+  uint8_t* ql = qh + q_stride;
+  if (GATHER_X) {
+    int t = row - P;
+    width = width_r;
+    if (row < P) {
+      const int p = sorted_pair[row];
+      t = (p >= 0 && p < P) ? p / k : -1;
+    }
+    if (t < 0) {
+      if (lane == 0) set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      for (int c = lane * 8; c < width; c += 256) {
+        *reinterpret_cast<uint2*>(qh + c) = make_uint2(0, 0);
+        *reinterpret_cast<uint2*>(ql + c) = make_uint2(0, 0);
+      }
+      if (lane == 0) scale[row] = 1.f;
+      return;
+    }
+    s = src + static_cast<size_t>(t) * src_stride;
+  } else {
+    s = src + static_cast<size_t>(row) * src_stride;
+    width = row < P ? width_r : width_s;
+  }
+  float amax = 0.f;
+  for (int c = lane * 8; c < width; c += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  float sc = 1.f;
+  if (amax > 0.f && isfinite(amax)) {
+    int e;
+    const float m = frexpf(amax * (1.0f / 448.0f), &e);   // amax/448 = m * 2^e, m in [0.5, 1)
+    sc = ldexpf(1.0f, m == 0.5f ? e - 1 : e);
+    if (amax / sc > 448.0f) sc *= 2.0f;
+  }
+  const float inv = 1.0f / sc;   // exact: sc is a power of two
+  for (int c = lane * 8; c < width; c += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hi[2] = {0, 0}, lo[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f2 = make_float2(__uint_as_float(w[i] << 16) * inv, __uint_as_float(w[i] & 0xffff0000u) * inv);
+      const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(f2, __NV_SATFINITE, __NV_E4M3);
+      const __half2_raw back = __nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3);
+      const float2 bf = __half22float2(__half2(back));
+      const float2 r2 = make_float2((f2.x - bf.x) * 16.0f, (f2.y - bf.y) * 16.0f);
+      const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(r2, __NV_SATFINITE, __NV_E4M3);
+      hi[i >> 1] |= static_cast<uint32_t>(h2) << (16 * (i & 1));
+      lo[i >> 1] |= static_cast<uint32_t>(l2) << (16 * (i & 1));
+    }
+    *reinterpret_cast<uint2*>(qh + c) = make_uint2(hi[0], hi[1]);
+    *reinterpret_cast<uint2*>(ql + c) = make_uint2(lo[0], lo[1]);
+  }
+  if (lane == 0) scale[row] = sc;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D byte matrix [rows][cols] (row pitch = cols bytes), box 128 bytes x box_rows,
+// 128-byte swizzle; rows past the end read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcPlan {
+  size_t xq, sx, h, hq, sh, total;
+  int TN;
+};
+
+TcPlan plan(const moe_config_t& c) {
+  const size_t P = static_cast<size_t>(c.T) * c.top_k, R = P + c.T;
+  const size_t fmax = std::max(c.d_ff, c.d_ff_shared);
+  TcPlan p;
+  size_t o = 0;
+  auto take = [&](size_t b) { size_t at = o; o += align_up(b, 1024); return at; };
+  p.xq = take(2 * R * c.d_model);
+  p.sx = take(4 * R);
+  p.h = take(2 * R * fmax);
+  p.hq = take(2 * R * fmax);
+  p.sh = take(4 * R);
+  p.total = o;
+  const double avg = static_cast<double>(P) / c.n_experts;
+  p.TN = avg <= 6 ? 8 : avg <= 12 ? 16 : avg <= 24 ? 32 : avg <= 48 ? 64 : 128;
+  return p;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUtensorMap& mB, TcArgs a,
+                        int wtiles_max, int num_sms, cudaStream_t stream) {
+  constexpr int NA = (MODE == 1) ? 2 : 1;
+  const int N = 2 * a.TN;
+  const int stage_bytes = NA * kABytes + align_up(static_cast<size_t>(N) * kBK, 1024);
+  a.stages = std::min(kMaxStages, kSmemBudget / stage_bytes);
+  const int per_acc = NA * N;
+  a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
+  int cols = 32;
+  while (cols < a.acc_bufs * per_acc) cols *= 2;
+  a.tmem_cols = cols;
+  size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + sizeof(TcCtrl);
+  smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
+  cudaError_t err = cudaFuncSetAttribute(ffn_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const long long tiles_ub =
+      static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
+  count_launches(1);
+  ffn_tc_kernel<MODE><<<grid, kTcThreads, smem, stream>>>(mA, mAS, mB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool ffn_tc_supported(const moe_config_t& c) {
+  return c.w_dtype == MOE_E4M3 && c.x_dtype == MOE_BF16 && c.d_ff % 128 == 0 && c.d_ff_shared % 128 == 0 &&
+         c.d_model % 128 == 0 && encode_fn() != nullptr;
+}
+
+size_t ffn_tc_ws_bytes(const moe_config_t& c) { return plan(c).total; }
+
+cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
+                          const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                          void* ws, unsigned* status, int num_sms, cudaStream_t stream) {
+  const int T = c.T, k = c.top_k, E = c.n_experts, d = c.d_model, f = c.d_ff, fs = c.d_ff_shared;
+  if (T == 0) return cudaSuccess;
+  const int P = T * k, R = P + T;
+  const int fmax = std::max(f, fs);
+  const TcPlan pl = plan(c);
+  char* base = static_cast<char*>(ws);
+  uint8_t* xq = reinterpret_cast<uint8_t*>(base + pl.xq);
+  float* sx = reinterpret_cast<float*>(base + pl.sx);
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(base + pl.h);
+  uint8_t* hq = reinterpret_cast<uint8_t*>(base + pl.hq);
+  float* sh = reinterpret_cast<float*>(base + pl.sh);
+
+  const int qblocks = ceil_div(R, 8);
+  count_launches(1);
+  quant2_rows_kernel<true><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d, d,
+                                                        d, xq, d, sx, status);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  CUtensorMap mA, mAS, mB;
+  TcArgs a = {};
+  a.offsets = offsets; a.sorted_pair = sorted_pair; a.topk_w = topk_w;
+  a.h = h; a.out_perm = out_perm; a.shared_out = shared_out;
+  a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
+  a.TN = pl.TN; a.status = status;
+
+  // gemm1: gate/up
+  if (!make_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, kBM) ||
+      !make_map(&mAS, w->s13, static_cast<uint64_t>(2) * fs, d, kBM) ||
+      !make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * pl.TN))
+    return cudaErrorInvalidValue;
+  a.a_scale = static_cast<const float*>(w->w13_scale);
+  a.as_scale = static_cast<const float*>(w->s13_scale);
+  a.b_scale = sx;
+  err = launch_gemm<1>(mA, mAS, mB, a, std::max(f, fs) / kBM, num_sms, stream);
+  if (err != cudaSuccess) return err;
+
+  count_launches(1);
+  quant2_rows_kernel<false><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P, T, k, f,
+                                                         fs, fmax, hq, fmax, sh, status);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  // gemm2: down projection, gate weight, outputs
+  if (!make_map(&mA, w->w2, static_cast<uint64_t>(E) * d, f, kBM) ||
+      !make_map(&mAS, w->s2, static_cast<uint64_t>(d), fs, kBM) ||
+      !make_map(&mB, hq, static_cast<uint64_t>(2) * R, fmax, 2 * pl.TN))
+    return cudaErrorInvalidValue;
+  a.a_scale = static_cast<const float*>(w->w2_scale);
+  a.as_scale = static_cast<const float*>(w->s2_scale);
+  a.b_scale = sh;
+  return launch_gemm<2>(mA, mAS, mB, a, d / kBM, num_sms, stream);
 }
 
 }  // namespace moe
