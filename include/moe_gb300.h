@@ -150,6 +150,33 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_permute for callers that cannot allocate device memory: same
+ * arguments and results as moe_permute, minus the workspace.  This entry
+ * point has no counterpart in the pages; it exists for integrations where
+ * device memory belongs to someone else -- a serving engine whose caching
+ * allocator or fixed budget must account for every byte, or a latency-
+ * critical loop in which a cudaMalloc (which can synchronise the device) is
+ * not allowed -- so the caller has no way to obtain a workspace to pass in.
+ *
+ * Its scratch is one 64 KiB array compiled into the library
+ * (MOE_NOALLOC_MAX_PAIRS = 65536 pairs x 256 experts of per-chunk counts and
+ * bases); every GPU that loads the library holds it until the process exits.
+ *   - Limit: T*k <= MOE_NOALLOC_MAX_PAIRS, else MOE_ERR_UNSUPPORTED is
+ *     returned before anything is launched.
+ *   - The first call on a device looks up the array's device address on
+ *     that device (a runtime query, no allocation); make that first call
+ *     before any stream capture is begun.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     every call overwrites all of the scratch it reads, so nothing needs to
+ *     be cleared between calls.  Calls whose kernels overlap on the GPU (for
+ *     example on two streams at once) race on the array: serialise them.
+ *   - No cudaMalloc, cudaFree or other allocating routine is ever called.
+ */
+#define MOE_NOALLOC_MAX_PAIRS 65536
+moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_ids, int32_t* expert_offsets,
+                                 int32_t* sorted_pair, int32_t* row_of, moe_stream_t stream);
+
+/*
  * Routed experts (grouped SwiGLU GEMMs) and the shared expert.
  * Sarvam blog, Table 1 rows "Routed expert compute" and "Shared expert
  * compute"; section "Scaling multilingual sovereign AI with MoE" (shared

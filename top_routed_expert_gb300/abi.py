@@ -18,6 +18,7 @@ from .build import LIB
 
 MOE_F32, MOE_BF16, MOE_E4M3, MOE_NVFP4 = 0, 1, 2, 3
 MOE_FLAG_SIMT_FFN = 0x1
+MOE_NOALLOC_MAX_PAIRS = 65536
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
@@ -27,7 +28,7 @@ STATUS = {
 
 # Every symbol include/moe_gb300.h declares.
 EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_route", "moe_permute",
-           "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_launch_count", "moe_get_device_status")
+           "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_launch_count", "moe_get_device_status")
 
 
 class MoEError(RuntimeError):
@@ -69,6 +70,7 @@ def load(path: str = LIB) -> ctypes.CDLL:
         "moe_workspace_bytes": (sz, [cfgp]),
         "moe_route": (i32, [cfgp, vp, vp, vp, vp, vp, vp]),
         "moe_permute": (i32, [cfgp, vp, vp, vp, vp, vp, sz, vp]),
+        "moe_permute_noalloc": (i32, [cfgp, vp, vp, vp, vp, vp]),
         "moe_expert_ffn": (i32, [cfgp, vp, vp, vp, vp, wp, vp, vp, vp, sz, vp]),
         "moe_combine": (i32, [cfgp, vp, vp, vp, vp, vp]),
         "moe_layer_forward": (i32, [cfgp, vp, vp, vp, wp, vp, vp, vp, vp, vp, sz, vp]),
@@ -133,6 +135,14 @@ def moe_permute(cfg, topk_ids, expert_offsets, sorted_pair, row_of, ws, stream=N
     _check(load().moe_permute(ctypes.byref(cfg), _ptr(topk_ids), _ptr(expert_offsets), _ptr(sorted_pair),
                               _ptr(row_of), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                               _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(cfg, topk_ids, expert_offsets, sorted_pair, row_of, stream=None):
+    """moe_permute without a workspace: its scratch is a fixed array inside the
+    library (at most MOE_NOALLOC_MAX_PAIRS = 65536 pairs; calls that overlap on
+    the GPU race on it)."""
+    _check(load().moe_permute_noalloc(ctypes.byref(cfg), _ptr(topk_ids), _ptr(expert_offsets),
+                                      _ptr(sorted_pair), _ptr(row_of), _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_expert_ffn(cfg, x, topk_w, expert_offsets, sorted_pair, weights: moe_weights_t, out_perm, shared_out, ws,

@@ -149,6 +149,18 @@ bool weights_ok(const moe_config_t& c, const moe_weights_t* w) {
 
 }  // namespace
 
+namespace moe {
+// Status word address and SM count of the current device (set up on first use).
+moe_status_t current_device(unsigned** status, int* num_sms) {
+  DeviceInfo di;
+  moe_status_t st = device_info(&di);
+  if (st != MOE_OK) return st;
+  *status = di.status;
+  *num_sms = di.num_sms;
+  return MOE_OK;
+}
+}  // namespace moe
+
 extern "C" {
 
 int moe_abi_version(void) { return MOE_ABI_VERSION; }

@@ -13,6 +13,8 @@
 // Deterministic and stable: within an expert the pairs come out in ascending
 // p, hence ascending token.  Ids outside [0, E) are skipped and recorded in
 // the device status word.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -129,4 +131,60 @@ cudaError_t launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, i
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (moe_permute_noalloc): the per-chunk counts and
+// bases live in a fixed array compiled into the library instead of a caller
+// workspace.  Sized for MOE_NOALLOC_MAX_PAIRS pairs and kPermMaxE experts:
+// two halves of (65536 / 2048 chunks) x 256 experts int32 = 64 KiB.
+constexpr int kNoAllocChunks = MOE_NOALLOC_MAX_PAIRS / kPermChunk;
+constexpr size_t kNoAllocHalfInts = static_cast<size_t>(kNoAllocChunks) * kPermMaxE;
+static __device__ __align__(256) int32_t g_permute_scratch[2 * kNoAllocHalfInts];
+
+static std::mutex g_scratch_mu;
+static void* g_scratch_addr[64] = {};
+
+// Device address of g_permute_scratch on the current device, looked up once
+// per device with that device current.
+static cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (err != cudaSuccess) return err;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+moe_status_t current_device(unsigned** status, int* num_sms);
+
 }  // namespace moe
+
+extern "C" moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_ids,
+                                            int32_t* expert_offsets, int32_t* sorted_pair, int32_t* row_of,
+                                            moe_stream_t stream) {
+  using namespace moe;
+  if (moe_workspace_bytes(cfg) == 0) return MOE_ERR_INVALID_ARG;   // full configuration check
+  const long long P = static_cast<long long>(cfg->T) * cfg->top_k;
+  if (P > MOE_NOALLOC_MAX_PAIRS) return MOE_ERR_UNSUPPORTED;
+  if (!expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (P > 0 && (!topk_ids || !sorted_pair || !row_of)) return MOE_ERR_INVALID_ARG;
+  // the two halves must be laid out exactly as launch_permute expects
+  static_assert(kNoAllocHalfInts * sizeof(int32_t) % 256 == 0, "scratch halves must stay 256-byte aligned");
+  if (permute_ws_bytes(static_cast<int>(P), cfg->n_experts) > sizeof(g_permute_scratch)) return MOE_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  int sms = 0;
+  moe_status_t st = current_device(&status, &sms);
+  if (st != MOE_OK) return st;
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_permute(topk_ids, static_cast<int>(P), cfg->n_experts, expert_offsets, sorted_pair, row_of, scratch,
+                        status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
