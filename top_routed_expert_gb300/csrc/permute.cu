@@ -110,6 +110,63 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int3
   }
 }
 
+// Whole permutation in one CTA when all pairs fit in one chunk (decode-sized
+// batches): histogram, scan and stable scatter without extra launches.
+__global__ void __launch_bounds__(kPermThreads)
+permute_small_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ offsets,
+                     int32_t* __restrict__ sorted_pair, int32_t* __restrict__ row_of, unsigned* status) {
+  constexpr int W = kPermThreads / 32;
+  __shared__ int run[kPermMaxE + 1];
+  __shared__ int wcnt[W][kPermMaxE];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < E; e += kPermThreads) run[e] = 0;
+  __syncthreads();
+  for (int p = tid; p < P; p += kPermThreads) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&run[e], 1);
+    else set_status(status, MOE_ERR_DEVICE_BOUNDS);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      const int c = run[e];
+      run[e] = acc;
+      offsets[e] = acc;
+      acc += c;
+    }
+    offsets[E] = acc;
+  }
+  __syncthreads();
+  for (int c0 = 0; c0 < P; c0 += kPermThreads) {
+    for (int i = tid; i < W * E; i += kPermThreads) wcnt[i / E][i % E] = 0;
+    __syncthreads();
+    const int p = c0 + tid;
+    int e = -1;
+    if (p < P) {
+      e = ids[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && rank_in_warp == 0) wcnt[warp][e] = __popc(same);
+    __syncthreads();
+    if (e >= 0) {
+      int pos = run[e] + rank_in_warp;
+      for (int w2 = 0; w2 < warp; ++w2) pos += wcnt[w2][e];
+      sorted_pair[pos] = p;
+      row_of[p] = pos;
+    }
+    __syncthreads();
+    for (int i = tid; i < E; i += kPermThreads) {
+      int s = 0;
+      for (int w2 = 0; w2 < W; ++w2) s += wcnt[w2][i];
+      run[i] += s;
+    }
+    __syncthreads();
+  }
+}
+
 size_t permute_ws_bytes(int P, int E) {
   const int nblk = ceil_div(P, kPermChunk);
   return 2 * align_up(sizeof(int32_t) * static_cast<size_t>(nblk) * E, 256);
@@ -123,6 +180,11 @@ cudaError_t launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, i
                                                  align_up(sizeof(int32_t) * static_cast<size_t>(nblk) * E, 256));
   if (P == 0) {
     return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), stream);
+  }
+  if (nblk == 1) {
+    count_launches(1);
+    permute_small_kernel<<<1, kPermThreads, 0, stream>>>(ids, P, E, offsets, sorted_pair, row_of, status);
+    return cudaGetLastError();
   }
   count_launches(3);
   permute_hist_kernel<<<nblk, kPermThreads, 0, stream>>>(ids, P, E, blk_counts, status);

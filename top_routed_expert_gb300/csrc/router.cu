@@ -16,7 +16,11 @@
 // dimension and the cluster's rank-0 CTA sums their partial logits out of
 // distributed shared memory in rank order (deterministic), adds the bias and
 // runs a warp-per-token register top-k (k rounds of a warp arg-max keyed on
-// (logit desc, index asc)).  Logits stay fp32 from bf16/fp32 inputs.
+// (logit desc, index asc)).  Inside a CTA one thread owns one expert (two when
+// E > 128) and keeps all TOK token sums in registers; chunks of W_r and x are
+// staged with cp.async, double-buffered, and read back as float4 (W_r rows
+// padded by 4 floats so a warp's 32 row reads spread over all banks; x reads
+// are broadcasts).  Logits stay fp32 from bf16/fp32 inputs.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -26,26 +30,56 @@ namespace cg = cooperative_groups;
 namespace moe {
 
 constexpr int kRouterThreads = 128;
-constexpr int kRouterKC = 32;          // hidden-dim chunk staged in shared memory
+constexpr int kRouterKC = 128;            // hidden-dim chunk per pipeline stage
+constexpr int kRouterWPitch = kRouterKC + 4;
 
-// TT tokens per thread (TOK = 8*TT per CTA), EPT experts per thread (E <= 16*EPT).
-template <typename XT, int TT, int EPT>
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <typename XT>
+struct XStage {          // x chunk row pitch in elements (16-byte aligned rows)
+  static constexpr int kPitch = kRouterKC + 16 / static_cast<int>(sizeof(XT));
+};
+
+__device__ __forceinline__ void x4_to_float(const float* p, float (&v)[4]) {
+  const float4 q = *reinterpret_cast<const float4*>(p);
+  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+__device__ __forceinline__ void x4_to_float(const uint16_t* p, float (&v)[4]) {
+  const uint2 q = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
+  v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
+}
+
+template <typename XT, int TOK, int EPT>
+struct RouterSmem {
+  static constexpr int EMAX = kRouterThreads * EPT;
+  static constexpr size_t kWStage = static_cast<size_t>(EMAX) * kRouterWPitch * sizeof(float);   // bytes
+  static constexpr size_t kXStage = (static_cast<size_t>(TOK) * XStage<XT>::kPitch * sizeof(XT) + 15) / 16 * 16;
+  static constexpr size_t kStage = kWStage + kXStage;
+  static constexpr size_t kPost = 2 * static_cast<size_t>(TOK) * EMAX * sizeof(float);
+};
+
+// TOK tokens per CTA, EPT experts per thread (E <= 128*EPT), NBUF staging buffers.
+template <typename XT, int TOK, int EPT, int NBUF>
 __global__ void __launch_bounds__(kRouterThreads)
 router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
               int T, int d, int E, int k, int kslice, int32_t* __restrict__ ids, float* __restrict__ gates,
               unsigned* status) {
-  constexpr int TOK = 8 * TT;
-  constexpr int EMAX = 16 * EPT;
-  // Dynamic shared memory, two phases:
-  //   main loop : wsm [EMAX][KC+1] | xs [TOK][KC+1]
-  //   reduction : lp  [TOK][EMAX] aliases wsm (this CTA's partial logits,
-  //               read by rank 0) | ls [TOK][EMAX+1] after xs (rank 0 sums)
-  extern __shared__ float smem_f[];
-  float (*wsm)[kRouterKC + 1] = reinterpret_cast<float (*)[kRouterKC + 1]>(smem_f);
-  float (*xs)[kRouterKC + 1] = reinterpret_cast<float (*)[kRouterKC + 1]>(smem_f + EMAX * (kRouterKC + 1));
-  float (*lp)[EMAX] = reinterpret_cast<float (*)[EMAX]>(smem_f);
-  float (*ls)[EMAX + 1] =
-      reinterpret_cast<float (*)[EMAX + 1]>(smem_f + EMAX * (kRouterKC + 1) + TOK * (kRouterKC + 1));
+  using L = RouterSmem<XT, TOK, EPT>;
+  constexpr int EMAX = L::EMAX;
+  constexpr int XP = XStage<XT>::kPitch;
+  extern __shared__ __align__(16) uint8_t smem_u8[];
+  // stage b: [W_r chunk EMAX x (KC+4) floats][x chunk TOK x XP]; after the
+  // main loop the area is reused for the partial and summed logits.
+  float* lp = reinterpret_cast<float*>(smem_u8);      // [TOK][EMAX] partial logits (read by rank 0)
+  float* ls = lp + TOK * EMAX;                         // [TOK][EMAX] rank 0: summed logits
 
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned S = cluster.num_blocks();
@@ -53,62 +87,95 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   const int tile = blockIdx.x / S;
   const int t0 = tile * TOK;
   const int tid = threadIdx.x;
-  const int tg = tid >> 4;       // token group: tokens tg*TT .. +TT-1
-  const int eg = tid & 15;       // experts eg + 16*i
-  const int kbeg = rank * kslice;
+  const int kbeg = min(d, static_cast<int>(rank) * kslice);
   const int kend = min(d, kbeg + kslice);
+  const int nchunks = (kend - kbeg) / kRouterKC;
 
-  float acc[TT][EPT];
-#pragma unroll
-  for (int a = 0; a < TT; ++a)
-#pragma unroll
-    for (int b = 0; b < EPT; ++b) acc[a][b] = 0.f;
+  auto wstage = [&](int buf) { return reinterpret_cast<float*>(smem_u8 + buf * L::kStage); };
+  auto xstage = [&](int buf) { return reinterpret_cast<XT*>(smem_u8 + buf * L::kStage + L::kWStage); };
 
-  for (int k0 = kbeg; k0 < kend; k0 += kRouterKC) {
-    // stage x[t0..t0+TOK)[k0..k0+KC) and W_r[0..E)[k0..k0+KC) as fp32
-    for (int i = tid; i < TOK * kRouterKC; i += kRouterThreads) {
-      const int r = i / kRouterKC, c = i % kRouterKC;
-      const int t = t0 + r;
-      xs[r][c] = (t < T) ? x_to_float<XT>(x[static_cast<size_t>(t) * d + k0 + c]) : 0.f;
-    }
+  auto stage_chunk = [&](int c, int buf) {
+    const int k0 = kbeg + c * kRouterKC;
+    float* wdst = wstage(buf);
     for (int i = tid; i < EMAX * (kRouterKC / 4); i += kRouterThreads) {
       const int r = i / (kRouterKC / 4), c4 = (i % (kRouterKC / 4)) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < E) v = *reinterpret_cast<const float4*>(wr + static_cast<size_t>(r) * d + k0 + c4);
-      wsm[r][c4 + 0] = v.x; wsm[r][c4 + 1] = v.y; wsm[r][c4 + 2] = v.z; wsm[r][c4 + 3] = v.w;
+      float* dst = wdst + r * kRouterWPitch + c4;
+      if (r < E) cp_async16(dst, wr + static_cast<size_t>(r) * d + k0 + c4);
+      else *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    XT* xdst = xstage(buf);
+    constexpr int EPC = 16 / static_cast<int>(sizeof(XT));   // elements per 16-byte piece
+    for (int i = tid; i < TOK * (kRouterKC / EPC); i += kRouterThreads) {
+      const int r = i / (kRouterKC / EPC), c = (i % (kRouterKC / EPC)) * EPC;
+      XT* dst = xdst + r * XP + c;
+      if (t0 + r < T) cp_async16(dst, x + static_cast<size_t>(t0 + r) * d + k0 + c);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+  };
+
+  float acc[EPT][TOK];
+#pragma unroll
+  for (int a = 0; a < EPT; ++a)
+#pragma unroll
+    for (int b = 0; b < TOK; ++b) acc[a][b] = 0.f;
+
+  if (nchunks > 0) stage_chunk(0, 0);
+  cp_async_commit();
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = (NBUF == 2) ? (c & 1) : 0;
+    if (NBUF == 2) {
+      if (c + 1 < nchunks) stage_chunk(c + 1, buf ^ 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kRouterKC; ++kk) {
-      float xv[TT], wv[EPT];
+    const float* wb = wstage(buf);
+    const XT* xb = xstage(buf);
+#pragma unroll 2
+    for (int kk = 0; kk < kRouterKC; kk += 4) {
+      float w[EPT][4];
 #pragma unroll
-      for (int a = 0; a < TT; ++a) xv[a] = xs[tg * TT + a][kk];
+      for (int a = 0; a < EPT; ++a) {
+        const float4 q = *reinterpret_cast<const float4*>(wb + (tid + kRouterThreads * a) * kRouterWPitch + kk);
+        w[a][0] = q.x; w[a][1] = q.y; w[a][2] = q.z; w[a][3] = q.w;
+      }
 #pragma unroll
-      for (int b = 0; b < EPT; ++b) wv[b] = wsm[eg + 16 * b][kk];
+      for (int b = 0; b < TOK; ++b) {
+        float xv[4];
+        x4_to_float(xb + b * XP + kk, xv);
 #pragma unroll
-      for (int a = 0; a < TT; ++a)
+        for (int a = 0; a < EPT; ++a)
 #pragma unroll
-        for (int b = 0; b < EPT; ++b) acc[a][b] = fmaf(xv[a], wv[b], acc[a][b]);
+          for (int q = 0; q < 4; ++q) acc[a][b] = fmaf(xv[q], w[a][q], acc[a][b]);
+      }
     }
     __syncthreads();
+    if (NBUF == 1 && c + 1 < nchunks) {
+      stage_chunk(c + 1, 0);
+      cp_async_commit();
+    }
   }
+  cp_async_wait<0>();
+  __syncthreads();
 
 #pragma unroll
-  for (int a = 0; a < TT; ++a)
+  for (int a = 0; a < EPT; ++a)
 #pragma unroll
-    for (int b = 0; b < EPT; ++b) lp[tg * TT + a][eg + 16 * b] = acc[a][b];
+    for (int b = 0; b < TOK; ++b) lp[b * EMAX + tid + kRouterThreads * a] = acc[a][b];
 
   cluster.sync();   // all partial logits of the cluster are in shared memory
   if (rank == 0) {
     for (int i = tid; i < TOK * EMAX; i += kRouterThreads) {
-      const int r = i / EMAX, e = i % EMAX;
+      const int e = i % EMAX;
       float s = 0.f;
       for (unsigned q = 0; q < S; ++q) {
-        const float* remote = cluster.map_shared_rank(&lp[0][0], q);
+        const float* remote = cluster.map_shared_rank(lp, q);
         s += remote[i];
       }
       if (e < E && bias) s += bias[e];
-      ls[r][e] = s;
+      ls[i] = s;
     }
   }
   cluster.sync();   // peers may exit only after rank 0 has read their partials
@@ -116,7 +183,7 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
 
   // Top-k: one warp per token.
   const int warp = tid >> 5, lane = tid & 31;
-  constexpr int EPL = EMAX / 32 > 0 ? EMAX / 32 : 1;   // experts per lane
+  constexpr int EPL = EMAX / 32;   // experts per lane
   for (int r = warp; r < TOK; r += kRouterThreads / 32) {
     const int t = t0 + r;
     if (t >= T) break;
@@ -125,7 +192,7 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (e < E) ? ls[r][e] : 0.f;
+      v[i] = (e < E) ? ls[r * EMAX + e] : 0.f;
       taken[i] = (e >= E);
     }
     float sel_v0 = 0.f, sum = 0.f;
@@ -163,29 +230,21 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   }
 }
 
-template <int TT, int EPT>
-constexpr size_t router_smem_bytes() {
-  return sizeof(float) * (static_cast<size_t>(16 * EPT) * (kRouterKC + 1) + 8 * TT * (kRouterKC + 1) +
-                          8 * TT * (16 * EPT + 1));
-}
-
-template <typename XT, int TT, int EPT>
-static cudaError_t launch_router_t(const void* x, const float* wr, const float* bias, int T, int d, int E,
-                                   int k, int S, int32_t* ids, float* w, unsigned* status,
-                                   cudaStream_t stream) {
-  constexpr int TOK = 8 * TT;
+template <typename XT, int TOK, int EPT, int NBUF>
+static cudaError_t launch_router_t(const void* x, const float* wr, const float* bias, int T, int d, int E, int k,
+                                   int S, int32_t* ids, float* w, unsigned* status, cudaStream_t stream) {
+  using L = RouterSmem<XT, TOK, EPT>;
   const int tiles = ceil_div(T, TOK);
   // hidden-dim slice per cluster rank, a multiple of the staging chunk
   const int kslice = ceil_div(ceil_div(d, S), kRouterKC) * kRouterKC;
+  constexpr size_t smem = (NBUF * L::kStage > L::kPost) ? NBUF * L::kStage : L::kPost;
+  static_assert(smem <= 227 * 1024, "router staging exceeds shared memory");
+  cudaError_t err = cudaFuncSetAttribute(router_kernel<XT, TOK, EPT, NBUF>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * S);
   cfg.blockDim = dim3(kRouterThreads);
-  constexpr size_t smem = router_smem_bytes<TT, EPT>();
-  static_assert(sizeof(float) * 16 * EPT * (kRouterKC + 1) >= sizeof(float) * 8 * TT * 16 * EPT,
-                "partial logits must fit in the weight staging area they alias");
-  cudaError_t err = cudaFuncSetAttribute(router_kernel<XT, TT, EPT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -196,12 +255,13 @@ static cudaError_t launch_router_t(const void* x, const float* wr, const float* 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launches(1);
-  return cudaLaunchKernelEx(&cfg, router_kernel<XT, TT, EPT>, static_cast<const XT*>(x), wr, bias, T, d, E,
+  return cudaLaunchKernelEx(&cfg, router_kernel<XT, TOK, EPT, NBUF>, static_cast<const XT*>(x), wr, bias, T, d, E,
                             k, kslice, ids, w, status);
 }
 
 // Chooses tokens-per-CTA and the cluster split so that small T still spreads
-// over the SMs: S ranks split d, up to 8 (the portable cluster size).
+// over the SMs: S ranks split d (up to 8, the portable cluster size), each rank
+// at least one staging chunk.
 cudaError_t launch_router(const void* x, bool x_bf16, const float* wr, const float* bias, int T, int d, int E,
                           int k, int32_t* ids, float* w, unsigned* status, int num_sms, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
@@ -209,15 +269,16 @@ cudaError_t launch_router(const void* x, bool x_bf16, const float* wr, const flo
   const int TOK = big ? 32 : 8;
   const int tiles = ceil_div(T, TOK);
   int S = 1;
-  while (S < 8 && tiles * S < 2 * num_sms && d / (2 * S) >= kRouterKC * 2) S *= 2;
+  while (S < 8 && tiles * S < num_sms && d / (2 * S) >= kRouterKC) S *= 2;
   const bool e128 = E <= 128;
-#define MOE_ROUTER_CASE(XT, TT, EPT) return launch_router_t<XT, TT, EPT>(x, wr, bias, T, d, E, k, S, ids, w, status, stream)
+#define MOE_ROUTER_CASE(XT, TOKC, EPT, NB) \
+  return launch_router_t<XT, TOKC, EPT, NB>(x, wr, bias, T, d, E, k, S, ids, w, status, stream)
   if (x_bf16) {
-    if (big) { if (e128) MOE_ROUTER_CASE(uint16_t, 4, 8); else MOE_ROUTER_CASE(uint16_t, 4, 16); }
-    else     { if (e128) MOE_ROUTER_CASE(uint16_t, 1, 8); else MOE_ROUTER_CASE(uint16_t, 1, 16); }
+    if (big) { if (e128) MOE_ROUTER_CASE(uint16_t, 32, 1, 2); else MOE_ROUTER_CASE(uint16_t, 32, 2, 1); }
+    else     { if (e128) MOE_ROUTER_CASE(uint16_t, 8, 1, 2); else MOE_ROUTER_CASE(uint16_t, 8, 2, 1); }
   } else {
-    if (big) { if (e128) MOE_ROUTER_CASE(float, 4, 8); else MOE_ROUTER_CASE(float, 4, 16); }
-    else     { if (e128) MOE_ROUTER_CASE(float, 1, 8); else MOE_ROUTER_CASE(float, 1, 16); }
+    if (big) { if (e128) MOE_ROUTER_CASE(float, 32, 1, 2); else MOE_ROUTER_CASE(float, 32, 2, 1); }
+    else     { if (e128) MOE_ROUTER_CASE(float, 8, 1, 2); else MOE_ROUTER_CASE(float, 8, 2, 1); }
   }
 #undef MOE_ROUTER_CASE
 }
