@@ -273,7 +273,7 @@ def measure(layer, x, cfg, steps, warmup, world, dev, gpu_index, abi, torch, clo
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        abi.moe_route(c, x, layer.w_router, layer.bias, ids, w, stream)
+        abi.moe_route(c, x, layer.w_router, layer.bias, ids, w, ws, stream)
         if ev is not None:
             ev[1].record(stream)
         abi.moe_permute(c, ids, offs, sp, row_of, ws, stream)

@@ -61,6 +61,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtyp
 
 /* Flags (moe_config_t.flags). */
 #define MOE_FLAG_SIMT_FFN 0x1u     /* run the expert FFN on the CUDA-core kernels */
+#define MOE_FLAG_SIMT_ROUTER 0x2u  /* run the router on the CUDA-core kernel       */
 
 typedef struct {
   int32_t T;            /* tokens, >= 0 (0 is a no-op)                          */
@@ -129,11 +130,15 @@ size_t moe_workspace_bytes(const moe_config_t* cfg);
  *   topk_ids    [T][k] int32 out: experts in descending logit order, ties to
  *               the lower index
  *   topk_w      [T][k] float out: renormalised gates (sum to one per token)
- * Uses no workspace.
+ *   ws, ws_bytes optional workspace.  With at least moe_workspace_bytes(cfg)
+ *               bytes, batches of >= 1024 bf16 tokens with E <= 128 run the
+ *               logits on the tensor cores (W_r split exactly into three bf16
+ *               terms held in the workspace); otherwise (or with ws NULL) the
+ *               CUDA-core router runs.  Both give fp32-accurate logits.
  */
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const float* w_router,
                        const float* expert_bias, int32_t* topk_ids, float* topk_w,
-                       moe_stream_t stream);
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * Permutation of the T*k (token, slot) pairs into per-expert groups, the

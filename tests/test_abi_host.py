@@ -54,26 +54,26 @@ def cfg(**kw):
     dict(T=-1), dict(d_model=100), dict(d_model=0), dict(d_model=32768), dict(n_experts=0),
     dict(n_experts=300), dict(top_k=0), dict(top_k=17), dict(n_experts=4, top_k=5), dict(d_ff=100),
     dict(d_ff_shared=0), dict(x_dtype=abi.MOE_E4M3), dict(w_dtype=abi.MOE_BF16), dict(y_dtype=abi.MOE_NVFP4),
-    dict(flags=0x80),
+    dict(flags=0x80), dict(flags=0x4),
 ])
 def test_invalid_config_rejected(lib, bad):
     c = cfg(**bad)
     assert lib.moe_workspace_bytes(ctypes.byref(c)) == 0
-    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None) == 1
+    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, 0, None) == 1
     assert lib.moe_layer_forward(ctypes.byref(c), None, None, None, None, None, None, None, None, None, 0,
                                  None) == 1
 
 
 def test_null_config_rejected(lib):
     assert lib.moe_workspace_bytes(None) == 0
-    assert lib.moe_route(None, None, None, None, None, None, None) == 1
+    assert lib.moe_route(None, None, None, None, None, None, None, 0, None) == 1
     assert lib.moe_combine(None, None, None, None, None, None) == 1
 
 
 def test_null_pointers_rejected(lib):
     c = cfg()
     fake = ctypes.c_void_p(0x10000)   # aligned, never dereferenced: validation fails first
-    assert lib.moe_route(ctypes.byref(c), None, fake, None, fake, fake, None) == 1
+    assert lib.moe_route(ctypes.byref(c), None, fake, None, fake, fake, None, 0, None) == 1
     assert lib.moe_combine(ctypes.byref(c), fake, None, fake, fake, None) == 1
     assert lib.moe_expert_ffn(ctypes.byref(c), fake, fake, fake, fake, None, fake, fake, fake, 1 << 40,
                               None) == 1
@@ -83,7 +83,7 @@ def test_misaligned_pointers_rejected(lib):
     c = cfg()
     ok = ctypes.c_void_p(0x10000)
     odd = ctypes.c_void_p(0x10002)
-    assert lib.moe_route(ctypes.byref(c), odd, ok, None, ok, ok, None) == 1
+    assert lib.moe_route(ctypes.byref(c), odd, ok, None, ok, ok, None, 0, None) == 1
     assert lib.moe_combine(ctypes.byref(c), ok, ok, ok, odd, None) == 1
 
 
@@ -114,7 +114,7 @@ def test_missing_weight_scales_rejected(lib):
 
 def test_zero_tokens_is_a_noop(lib):
     c = cfg(T=0)
-    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None) == 0
+    assert lib.moe_route(ctypes.byref(c), None, None, None, None, None, None, 0, None) == 0
     assert lib.moe_combine(ctypes.byref(c), None, None, None, None, None) == 0
     assert lib.moe_layer_forward(ctypes.byref(c), None, None, None, None, None, None, None, None, None, 0,
                                  None) == 0
@@ -135,4 +135,4 @@ def test_no_cuda_device_reports_error(lib):
         pytest.skip("a GPU is present")
     c = cfg()
     fake = ctypes.c_void_p(0x10000)
-    assert lib.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, None) in (4, 7)
+    assert lib.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, None, 0, None) in (4, 7)

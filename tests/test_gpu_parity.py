@@ -113,7 +113,7 @@ def test_stepwise_calls_match_layer_forward():
     shared = torch.empty((T, d), dtype=torch.float32, device=dev)
     y = torch.empty((T, d), dtype=torch.float32, device=dev)
     ws = layer.workspace()
-    abi.moe_route(cfg, x, layer.w_router, layer.bias, ids, w)
+    abi.moe_route(cfg, x, layer.w_router, layer.bias, ids, w, ws)
     abi.moe_permute(cfg, ids, offs, sp, row_of, ws)
     abi.moe_expert_ffn(cfg, x, w, offs, sp, layer.weights, out_perm, shared, ws)
     abi.moe_combine(cfg, out_perm, row_of, shared, y)
@@ -180,7 +180,7 @@ def test_router_alone_with_bias():
     cfg = layer.config()
     ids = torch.empty((77, 5), dtype=torch.int32, device="cuda")
     w = torch.empty((77, 5), dtype=torch.float32, device="cuda")
-    abi.moe_route(cfg, device_x(inp), layer.w_router, layer.bias, ids, w)
+    abi.moe_route(cfg, device_x(inp), layer.w_router, layer.bias, ids, w, layer.workspace())
     assert abi.moe_get_device_status() == 0
     ids_np, w_np = ids.cpu().numpy(), w.cpu().numpy()
     _, o = check_routing(inp, ids_np, w_np, oracle.permute(ids_np, 64)[1])
@@ -216,3 +216,41 @@ def test_tensor_core_matches_simt_closely():
     assert np.array_equal(ids_tc, ids_s)
     rel = np.linalg.norm(y_tc - y_s) / np.linalg.norm(y_s)
     assert rel < 3e-3, rel
+
+
+@pytest.mark.parametrize("T,E,k", [(1100, 96, 5), (1024, 128, 8), (2049, 128, 6)])
+def test_tensor_core_router_ragged(T, E, k):
+    # >= 1024 bf16 tokens and E <= 128 select the tensor-core router; a ragged
+    # last 64-token tile, an E that leaves padded expert rows, and a bias
+    inp = moe_synth.make_custom(T=T, d=512, E=E, k=k, f=128, fs=128, x_dtype="bf16", w_dtype="e4m3", seed=T)
+    inp.bias = np.random.default_rng(T).standard_normal(E).astype(np.float32) * 0.5
+    layer = MoELayer(inp)
+    cfg = layer.config()
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    abi.moe_route(cfg, device_x(inp), layer.w_router, layer.bias, ids, w, layer.workspace())
+    assert abi.moe_get_device_status() == 0
+    ids_np, w_np = ids.cpu().numpy(), w.cpu().numpy()
+    check_routing(inp, ids_np, w_np, oracle.permute(ids_np, E)[1])
+
+
+def test_tensor_core_router_matches_cuda_core_router():
+    inp = workload("prefill")
+    out = []
+    for flags in (0, abi.MOE_FLAG_SIMT_ROUTER):
+        layer = MoELayer(inp, flags=flags)
+        cfg = layer.config()
+        T, k = inp.cfg.T, inp.cfg.k
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        abi.moe_route(cfg, device_x(inp), layer.w_router, layer.bias, ids, w, layer.workspace())
+        assert abi.moe_get_device_status() == 0
+        out.append((ids.cpu().numpy(), w.cpu().numpy()))
+    (i0, w0), (i1, w1) = out
+    L = oracle.router_logits(oracle.x_values(inp), inp.w_router, None)
+    sel, order = oracle.near_ties(L, inp.cfg.k)
+    clean = ~sel & ~order
+    assert np.array_equal(i0[clean], i1[clean])
+    assert np.max(np.abs(w0[clean] - w1[clean])) < 1e-5
+    for ids_np, w_np in out:
+        check_routing(inp, ids_np, w_np, oracle.permute(ids_np, inp.cfg.E)[1])

@@ -18,6 +18,7 @@ from .build import LIB
 
 MOE_F32, MOE_BF16, MOE_E4M3, MOE_NVFP4 = 0, 1, 2, 3
 MOE_FLAG_SIMT_FFN = 0x1
+MOE_FLAG_SIMT_ROUTER = 0x2
 MOE_NOALLOC_MAX_PAIRS = 65536
 
 STATUS = {
@@ -68,7 +69,7 @@ def load(path: str = LIB) -> ctypes.CDLL:
         "moe_abi_version": (i32, []),
         "moe_status_str": (ctypes.c_char_p, [i32]),
         "moe_workspace_bytes": (sz, [cfgp]),
-        "moe_route": (i32, [cfgp, vp, vp, vp, vp, vp, vp]),
+        "moe_route": (i32, [cfgp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_permute": (i32, [cfgp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_permute_noalloc": (i32, [cfgp, vp, vp, vp, vp, vp]),
         "moe_expert_ffn": (i32, [cfgp, vp, vp, vp, vp, wp, vp, vp, vp, sz, vp]),
@@ -126,9 +127,10 @@ def moe_workspace_bytes(cfg: moe_config_t) -> int:
     return load().moe_workspace_bytes(ctypes.byref(cfg))
 
 
-def moe_route(cfg, x, w_router, expert_bias, topk_ids, topk_w, stream=None):
+def moe_route(cfg, x, w_router, expert_bias, topk_ids, topk_w, ws=None, stream=None):
     _check(load().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(expert_bias), _ptr(topk_ids),
-                            _ptr(topk_w), _stream(stream)), "moe_route")
+                            _ptr(topk_w), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                            _stream(stream)), "moe_route")
 
 
 def moe_permute(cfg, topk_ids, expert_offsets, sorted_pair, row_of, ws, stream=None):

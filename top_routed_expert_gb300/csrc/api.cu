@@ -12,6 +12,10 @@ namespace moe {
 // launchers (one per translation unit)
 cudaError_t launch_router(const void* x, bool x_bf16, const float* wr, const float* bias, int T, int d, int E,
                           int k, int32_t* ids, float* w, unsigned* status, int num_sms, cudaStream_t stream);
+bool router_tc_supported(int T, int d, int E, bool x_bf16);
+size_t router_tc_ws_bytes(int d);
+cudaError_t launch_router_tc(const void* x, const float* wr, const float* bias, int T, int d, int E, int k,
+                             int32_t* ids, float* w, void* ws, unsigned* status, int num_sms, cudaStream_t stream);
 size_t permute_ws_bytes(int P, int E);
 cudaError_t launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, int32_t* sorted_pair,
                            int32_t* row_of, void* ws, unsigned* status, cudaStream_t stream);
@@ -93,12 +97,16 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_E4M3 && c->w_dtype != MOE_NVFP4) return MOE_ERR_INVALID_ARG;
   if (c->y_dtype != MOE_F32 && c->y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(c->T) * c->top_k > (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~MOE_FLAG_SIMT_FFN) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER)) != 0) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
 bool use_tc(const moe_config_t& c) {
   return !(c.flags & MOE_FLAG_SIMT_FFN) && ffn_tc_supported(c);
+}
+
+bool use_tc_router(const moe_config_t& c) {
+  return !(c.flags & MOE_FLAG_SIMT_ROUTER) && router_tc_supported(c.T, c.d_model, c.n_experts, c.x_dtype == MOE_BF16);
 }
 
 size_t ffn_ws_bytes(const moe_config_t& c) {
@@ -124,7 +132,9 @@ FwdPlan plan_forward(const moe_config_t& c) {
   p.row_of = take(sizeof(int32_t) * P);
   p.out_perm = take(sizeof(float) * P * c.d_model);
   p.shared_out = take(sizeof(float) * static_cast<size_t>(c.T) * c.d_model);
-  p.scratch = take(std::max(permute_ws_bytes(static_cast<int>(P), c.n_experts), ffn_ws_bytes(c)));
+  size_t scratch = std::max(permute_ws_bytes(static_cast<int>(P), c.n_experts), ffn_ws_bytes(c));
+  if (use_tc_router(c)) scratch = std::max(scratch, router_tc_ws_bytes(c.d_model));
+  p.scratch = take(scratch);
   p.total = o;
   return p;
 }
@@ -186,7 +196,7 @@ size_t moe_workspace_bytes(const moe_config_t* cfg) {
 }
 
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const float* w_router, const float* expert_bias,
-                       int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+                       int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
   if (cfg->T == 0) return MOE_OK;
@@ -194,8 +204,13 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const float* w_ro
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) ||
       (expert_bias && !aligned(expert_bias, 4)))
     return MOE_ERR_INVALID_ARG;
+  if (ws && !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
   DeviceInfo di;
   if ((st = device_info(&di)) != MOE_OK) return st;
+  if (use_tc_router(*cfg) && ws && ws_bytes >= router_tc_ws_bytes(cfg->d_model))
+    return cuda_status(launch_router_tc(x, w_router, expert_bias, cfg->T, cfg->d_model, cfg->n_experts, cfg->top_k,
+                                        topk_ids, topk_w, ws, di.status, di.num_sms,
+                                        static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_router(x, cfg->x_dtype == MOE_BF16, w_router, expert_bias, cfg->T, cfg->d_model,
                                    cfg->n_experts, cfg->top_k, topk_ids, topk_w, di.status, di.num_sms,
                                    static_cast<cudaStream_t>(stream)));
@@ -283,7 +298,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const flo
   float* shared_out = reinterpret_cast<float*>(base + p.shared_out);
   void* scratch = base + p.scratch;
   const size_t scratch_bytes = p.total - p.scratch;
-  if ((st = moe_route(cfg, x, w_router, expert_bias, ids, w, stream)) != MOE_OK) return st;
+  if ((st = moe_route(cfg, x, w_router, expert_bias, ids, w, scratch, scratch_bytes, stream)) != MOE_OK) return st;
   if ((st = moe_permute(cfg, ids, offsets, sorted_pair, row_of, scratch, scratch_bytes, stream)) != MOE_OK)
     return st;
   if ((st = moe_expert_ffn(cfg, x, w, offsets, sorted_pair, weights, out_perm, shared_out, scratch, scratch_bytes,

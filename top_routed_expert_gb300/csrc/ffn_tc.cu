@@ -72,8 +72,10 @@ struct __align__(16) TcCtrl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t ep_sync;            // the four epilogue warps meet here once per tile (count 128)
   uint32_t tmem_base;
   int abort;
+  float coef[2][kBM];          // per-row epilogue coefficient, double-buffered by tile parity
   GroupTable gt;
 };
 
@@ -118,6 +120,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       mbar_init(smem_u32(&c->tempty[b]), 128);
     }
     mbar_init(smem_u32(&c->drain), 1);
+    mbar_init(smem_u32(&c->ep_sync), 128);
     c->abort = 0;
     fence_barrier_init();
     // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
@@ -256,12 +259,40 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     // -------------------------------------------------- epilogue (warps 2..5)
     const int sub = warp & 3;                       // TMEM lanes this warp may access
     const int n = sub * 32 + lane;                  // weight row within the tile
+    const int et = threadIdx.x - 64;                // 0..127 across the four epilogue warps
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
-    int ab = 0;
-    uint32_t aph = 0;
+    int ab = 0, cb_par = 0;
+    uint32_t aph = 0, eph = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
       const Tile t = decode_tile(c->gt, G, i, a.TN);
       const bool shr = t.g == a.E;
+      // Per-row coefficients of this tile, one row per epilogue thread, loaded
+      // while the MMAs run: the row's activation scale, times the gate weight
+      // of its (token, slot) pair in the down projection.
+      {
+        float cf = 0.f;
+        if (et < t.nrows) {
+          const int row = t.row0 + et;
+          cf = a.b_scale[row];
+          if (MODE == 2 && !shr) {
+            const int p = a.sorted_pair[row];
+            if (p >= 0 && p < a.P) {
+              cf *= a.topk_w[p];
+            } else {
+              cf = 0.f;
+              set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+            }
+          }
+        }
+        c->coef[cb_par][et] = cf;
+      }
+      // all four warps' coefficients written (bounded wait: a warp that gave up
+      // cannot leave the others blocked)
+      mbar_arrive(smem_u32(&c->ep_sync));
+      if (!mbar_wait(smem_u32(&c->ep_sync), eph, abort, kWaitLimitNs)) break;
+      eph ^= 1u;
+      const float* coef = c->coef[cb_par];
+      cb_par ^= 1;
       if (!mbar_wait(smem_u32(&c->tfull[ab]), aph, abort, kWaitLimitNs)) break;
       tc_fence_after();
       if (MODE == 1) {
@@ -270,16 +301,15 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const float sg = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + col];
         const float su = shr ? a.as_scale[width + col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + a.f + col];
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
-        for (int c0 = 0; c0 < N; c0 += 16) {
-          float gv[16], uv[16];
-          tmem_ld16(cb + c0, gv);
-          tmem_ld16(cb + N + c0, uv);
+        for (int c0 = 0; c0 < N; c0 += 32) {   // N is a multiple of 16; a 32-wide load past N stays in this buffer
+          float gv[32], uv[32];
+          tmem_ld32x2(cb + c0, cb + N + c0, gv, uv);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
+          for (int jj = 0; jj < 16; ++jj) {
             const int j = c0 / 2 + jj;
             if (j < t.nrows) {
               const int row = t.row0 + j;
-              const float sx = a.b_scale[row];
+              const float sx = coef[j];
               const float g = (gv[2 * jj] + gv[2 * jj + 1] * 0.0625f) * sx * sg;
               const float u = (uv[2 * jj] + uv[2 * jj + 1] * 0.0625f) * sx * su;
               a.h[static_cast<size_t>(row) * a.fmax + col] = __float2bfloat16_rn(silu(g) * u);
@@ -290,24 +320,19 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const int col = t.wt * kBM + n;
         const float sw = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * a.d + col];
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
-        for (int c0 = 0; c0 < N; c0 += 16) {
-          float dv[16];
-          tmem_ld16(cb + c0, dv);
+        for (int c0 = 0; c0 < N; c0 += 64) {
+          float d0[32], d1[32];
+          tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
+          for (int jj = 0; jj < 32; ++jj) {
             const int j = c0 / 2 + jj;
+            const float* dv = jj < 16 ? d0 : d1;
+            const int q = 2 * (jj & 15);
             if (j < t.nrows) {
               const int row = t.row0 + j;
-              const float o = (dv[2 * jj] + dv[2 * jj + 1] * 0.0625f) * a.b_scale[row] * sw;
-              if (shr) {
-                a.shared_out[static_cast<size_t>(row - a.P) * a.d + col] = o;
-              } else {
-                const int p = a.sorted_pair[row];
-                float gw = 0.f;
-                if (p >= 0 && p < a.P) gw = a.topk_w[p];
-                else if (lane == 0) set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
-                a.out_perm[static_cast<size_t>(row) * a.d + col] = o * gw;
-              }
+              const float o = (dv[q] + dv[q + 1] * 0.0625f) * coef[j] * sw;
+              if (shr) a.shared_out[static_cast<size_t>(row - a.P) * a.d + col] = o;
+              else a.out_perm[static_cast<size_t>(row) * a.d + col] = o;
             }
           }
         }
@@ -475,8 +500,14 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUt
   a.stages = std::min(kMaxStages, kSmemBudget / stage_bytes);
   const int per_acc = NA * N;
   a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
+  // The epilogue reads 32 columns per load (gemm1: gate and up from column c0
+  // and N + c0, c0 < N in steps of 32; gemm2: 64 from c0, c0 < N in steps of
+  // 64), so the allocation covers the last buffer plus that overhang.
+  const int last = (a.acc_bufs - 1) * per_acc;
+  const int reach = (MODE == 1) ? last + N + (N + 31) / 32 * 32 : last + (N + 63) / 64 * 64;
   int cols = 32;
-  while (cols < a.acc_bufs * per_acc) cols *= 2;
+  while (cols < reach) cols *= 2;
+  if (cols > 512) return cudaErrorInvalidConfiguration;
   a.tmem_cols = cols;
   size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + sizeof(TcCtrl);
   smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
@@ -532,11 +563,12 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   // gemm1: gate/up
   if (!make_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, kBM) ||
       !make_map(&mAS, w->s13, static_cast<uint64_t>(2) * fs, d, kBM) ||
-      !make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * pl.TN))
+      !make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * std::min(pl.TN, 64)))
     return cudaErrorInvalidValue;
   a.a_scale = static_cast<const float*>(w->w13_scale);
   a.as_scale = static_cast<const float*>(w->s13_scale);
   a.b_scale = sx;
+  a.TN = std::min(pl.TN, 64);   // 2 x (gate, up) x 2*TN columns must fit TMEM twice over
   err = launch_gemm<1>(mA, mAS, mB, a, std::max(f, fs) / kBM, num_sms, stream);
   if (err != cudaSuccess) return err;
 
@@ -554,6 +586,7 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   a.a_scale = static_cast<const float*>(w->w2_scale);
   a.as_scale = static_cast<const float*>(w->s2_scale);
   a.b_scale = sh;
+  a.TN = pl.TN;
   return launch_gemm<2>(mA, mAS, mB, a, d / kBM, num_sms, stream);
 }
 

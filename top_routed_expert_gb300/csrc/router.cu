@@ -24,6 +24,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "topk.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -183,50 +184,11 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
 
   // Top-k: one warp per token.
   const int warp = tid >> 5, lane = tid & 31;
-  constexpr int EPL = EMAX / 32;   // experts per lane
   for (int r = warp; r < TOK; r += kRouterThreads / 32) {
     const int t = t0 + r;
     if (t >= T) break;
-    float v[EPL];
-    bool taken[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? ls[r * EMAX + e] : 0.f;
-      taken[i] = (e >= E);
-    }
-    float sel_v0 = 0.f, sum = 0.f;
-    float my_z = 0.f;        // lane j keeps slot j's unnormalised gate
-    int my_e = 0;
-    bool bad = false;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      if (be == 0x7fffffff || !isfinite(bv)) { bad = true; be = 0; bv = 0.f; }
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i == be) taken[i] = true;
-      if (j == 0) sel_v0 = bv;
-      const float z = expf(bv - sel_v0);
-      sum += z;
-      if (lane == j) { my_z = z; my_e = be; }
-    }
-    if (bad && lane == 0) set_status(status, MOE_ERR_DEVICE_NONFINITE);
-    if (lane < k) {
-      ids[static_cast<size_t>(t) * k + lane] = my_e;
-      gates[static_cast<size_t>(t) * k + lane] = my_z / sum;
-    }
+    warp_topk_token<EMAX / 32>(ls + r * EMAX, E, k, lane, ids + static_cast<size_t>(t) * k,
+                               gates + static_cast<size_t>(t) * k, status);
   }
 }
 
