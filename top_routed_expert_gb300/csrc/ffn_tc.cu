@@ -34,7 +34,8 @@ namespace moe {
 
 using namespace ptx;
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;          // producer, MMA, 8 epilogue warps
+constexpr int kEpiThreads = 256;
 constexpr int kBK = 128;                // K bytes (= FP8 elements) per pipeline stage
 constexpr int kBM = 128;                // weight rows per tile = MMA M
 constexpr int kMaxStages = 8;
@@ -42,6 +43,18 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: no legitimate wait co
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
 constexpr uint32_t kABytes = kBM * kBK;            // 16 KB per weight tile
 constexpr int kSmemBudget = 220 * 1024;
+
+// Tuning knobs (compile-time): largest token tile of the gate/up and of the
+// down GEMM, and the L2 promotion of the TMA loads.
+#ifndef MOE_TC_TN1_CAP
+#define MOE_TC_TN1_CAP 64
+#endif
+#ifndef MOE_TC_TN2_CAP
+#define MOE_TC_TN2_CAP 128
+#endif
+#ifndef MOE_TC_L2_PROMOTION
+#define MOE_TC_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
 
 struct TcArgs {
   const int32_t* offsets;      // [E+1]
@@ -72,7 +85,7 @@ struct __align__(16) TcCtrl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
-  uint64_t ep_sync;            // the four epilogue warps meet here once per tile (count 128)
+  uint64_t ep_sync;            // the eight epilogue warps meet here once per tile
   uint32_t tmem_base;
   int abort;
   float coef[2][kBM];          // per-row epilogue coefficient, double-buffered by tile parity
@@ -117,10 +130,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&c->tfull[b]), 1);
-      mbar_init(smem_u32(&c->tempty[b]), 128);
+      mbar_init(smem_u32(&c->tempty[b]), kEpiThreads);
     }
     mbar_init(smem_u32(&c->drain), 1);
-    mbar_init(smem_u32(&c->ep_sync), 128);
+    mbar_init(smem_u32(&c->ep_sync), kEpiThreads);
     c->abort = 0;
     fence_barrier_init();
     // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
@@ -256,20 +269,23 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       mbar_wait(smem_u32(&c->drain), 0, &no_abort, kDrainLimitNs);
     }
   } else {
-    // -------------------------------------------------- epilogue (warps 2..5)
-    const int sub = warp & 3;                       // TMEM lanes this warp may access
+    // -------------------------------------------------- epilogue (warps 2..9)
+    // Two warps per TMEM sub-partition (warp % 4 selects the 32 lanes a warp
+    // may read); the pair of warps splits the tile's column chunks.
+    const int sub = warp & 3;
+    const int half = (warp - 2) >> 2;               // 0 or 1
     const int n = sub * 32 + lane;                  // weight row within the tile
-    const int et = threadIdx.x - 64;                // 0..127 across the four epilogue warps
+    const int et = threadIdx.x - 64;                // 0..255 across the epilogue warps
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
     int ab = 0, cb_par = 0;
     uint32_t aph = 0, eph = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
       const Tile t = decode_tile(c->gt, G, i, a.TN);
       const bool shr = t.g == a.E;
-      // Per-row coefficients of this tile, one row per epilogue thread, loaded
-      // while the MMAs run: the row's activation scale, times the gate weight
-      // of its (token, slot) pair in the down projection.
-      {
+      // Per-row coefficients of this tile, loaded while the MMAs run: the
+      // row's activation scale, times the gate weight of its (token, slot)
+      // pair in the down projection.
+      if (et < kBM) {
         float cf = 0.f;
         if (et < t.nrows) {
           const int row = t.row0 + et;
@@ -286,8 +302,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         }
         c->coef[cb_par][et] = cf;
       }
-      // all four warps' coefficients written (bounded wait: a warp that gave up
-      // cannot leave the others blocked)
+      // all coefficients written (bounded wait: a warp that gave up cannot
+      // leave the others blocked)
       mbar_arrive(smem_u32(&c->ep_sync));
       if (!mbar_wait(smem_u32(&c->ep_sync), eph, abort, kWaitLimitNs)) break;
       eph ^= 1u;
@@ -295,44 +311,48 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       cb_par ^= 1;
       if (!mbar_wait(smem_u32(&c->tfull[ab]), aph, abort, kWaitLimitNs)) break;
       tc_fence_after();
+      const int col = t.wt * kBM + n;
       if (MODE == 1) {
         const int width = shr ? a.fs : a.f;
-        const int col = t.wt * kBM + n;
         const float sg = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + col];
         const float su = shr ? a.as_scale[width + col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + a.f + col];
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
-        for (int c0 = 0; c0 < N; c0 += 32) {   // N is a multiple of 16; a 32-wide load past N stays in this buffer
-          float gv[32], uv[32];
+        // chunks of 32 columns = 16 token rows; N is a multiple of 16 and a
+        // 32-wide load past N stays inside the allocation
+        for (int c0 = 32 * half; c0 < N; c0 += 64) {
+          float gv[32], uv[32], cf[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) cf[jj] = coef[c0 / 2 + jj];
           tmem_ld32x2(cb + c0, cb + N + c0, gv, uv);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = c0 / 2 + jj;
             if (j < t.nrows) {
               const int row = t.row0 + j;
-              const float sx = coef[j];
-              const float g = (gv[2 * jj] + gv[2 * jj + 1] * 0.0625f) * sx * sg;
-              const float u = (uv[2 * jj] + uv[2 * jj + 1] * 0.0625f) * sx * su;
+              const float g = (gv[2 * jj] + gv[2 * jj + 1] * 0.0625f) * cf[jj] * sg;
+              const float u = (uv[2 * jj] + uv[2 * jj + 1] * 0.0625f) * cf[jj] * su;
               a.h[static_cast<size_t>(row) * a.fmax + col] = __float2bfloat16_rn(silu(g) * u);
             }
           }
         }
       } else {
-        const int col = t.wt * kBM + n;
         const float sw = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * a.d + col];
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
-        for (int c0 = 0; c0 < N; c0 += 64) {
-          float d0[32], d1[32];
+        float* outb = shr ? a.shared_out + (static_cast<size_t>(t.row0 - a.P) * a.d + col)
+                          : a.out_perm + (static_cast<size_t>(t.row0) * a.d + col);
+        // chunks of 64 columns = 32 token rows
+        for (int c0 = 64 * half; c0 < N; c0 += 128) {
+          float d0[32], d1[32], cf[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) cf[jj] = coef[c0 / 2 + jj];
           tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             const int j = c0 / 2 + jj;
-            const float* dv = jj < 16 ? d0 : d1;
-            const int q = 2 * (jj & 15);
             if (j < t.nrows) {
-              const int row = t.row0 + j;
-              const float o = (dv[q] + dv[q + 1] * 0.0625f) * coef[j] * sw;
-              if (shr) a.shared_out[static_cast<size_t>(row - a.P) * a.d + col] = o;
-              else a.out_perm[static_cast<size_t>(row) * a.d + col] = o;
+              const float* dv = jj < 16 ? d0 : d1;
+              const int q = 2 * (jj & 15);
+              outb[static_cast<size_t>(j) * a.d] = (dv[q] + dv[q + 1] * 0.0625f) * cf[jj] * sw;
             }
           }
         }
@@ -465,7 +485,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, MOE_TC_L2_PROMOTION,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -563,12 +583,12 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   // gemm1: gate/up
   if (!make_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, kBM) ||
       !make_map(&mAS, w->s13, static_cast<uint64_t>(2) * fs, d, kBM) ||
-      !make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * std::min(pl.TN, 64)))
+      !make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * std::min(pl.TN, MOE_TC_TN1_CAP)))
     return cudaErrorInvalidValue;
   a.a_scale = static_cast<const float*>(w->w13_scale);
   a.as_scale = static_cast<const float*>(w->s13_scale);
   a.b_scale = sx;
-  a.TN = std::min(pl.TN, 64);   // 2 x (gate, up) x 2*TN columns must fit TMEM twice over
+  a.TN = std::min(pl.TN, MOE_TC_TN1_CAP);   // 2 x (gate, up) x 2*TN columns fit TMEM twice over at 64
   err = launch_gemm<1>(mA, mAS, mB, a, std::max(f, fs) / kBM, num_sms, stream);
   if (err != cudaSuccess) return err;
 
@@ -581,12 +601,12 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   // gemm2: down projection, gate weight, outputs
   if (!make_map(&mA, w->w2, static_cast<uint64_t>(E) * d, f, kBM) ||
       !make_map(&mAS, w->s2, static_cast<uint64_t>(d), fs, kBM) ||
-      !make_map(&mB, hq, static_cast<uint64_t>(2) * R, fmax, 2 * pl.TN))
+      !make_map(&mB, hq, static_cast<uint64_t>(2) * R, fmax, 2 * std::min(pl.TN, MOE_TC_TN2_CAP)))
     return cudaErrorInvalidValue;
   a.a_scale = static_cast<const float*>(w->w2_scale);
   a.as_scale = static_cast<const float*>(w->s2_scale);
   a.b_scale = sh;
-  a.TN = pl.TN;
+  a.TN = std::min(pl.TN, MOE_TC_TN2_CAP);
   return launch_gemm<2>(mA, mAS, mB, a, d / kBM, num_sms, stream);
 }
 
