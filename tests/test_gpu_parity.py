@@ -198,19 +198,21 @@ TC_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("w_dtype", ["e4m3", "nvfp4"])
 @pytest.mark.parametrize("shape", TC_SHAPES, ids=[f"T{s['T']}_E{s['E']}" for s in TC_SHAPES])
-def test_tensor_core_path_tiles(shape):
-    inp = moe_synth.make_custom(x_dtype="bf16", w_dtype="e4m3", seed=shape["T"], **shape)
+def test_tensor_core_path_tiles(shape, w_dtype):
+    inp = moe_synth.make_custom(x_dtype="bf16", w_dtype=w_dtype, seed=shape["T"], **shape)
     _, _, y, ids, w, offs = run_layer(inp)
     check_routing(inp, ids, w, offs)
     check_output(inp, y, ids)
 
 
-def test_tensor_core_matches_simt_closely():
-    # both paths against each other on the decode workload: the two-term FP8
-    # activation split keeps the tensor-core result within bf16-rounding
-    # distance of the fp32 CUDA-core result
-    inp = workload("decode")
+@pytest.mark.parametrize("name", ["decode", "100b_decode"])
+def test_tensor_core_matches_simt_closely(name):
+    # both paths against each other: the exact activation encodings (two E4M3
+    # terms, or scaled f16) keep the tensor-core result within bf16-rounding
+    # distance (H is rounded to bf16 once) of the fp32 CUDA-core result
+    inp = workload(name)
     _, _, y_tc, ids_tc, _, _ = run_layer(inp, 0)
     _, _, y_s, ids_s, _, _ = run_layer(inp, abi.MOE_FLAG_SIMT_FFN)
     assert np.array_equal(ids_tc, ids_s)

@@ -29,6 +29,11 @@ size_t ffn_tc_ws_bytes(const moe_config_t& c);
 cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                           const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
                           void* ws, unsigned* status, int num_sms, cudaStream_t stream);
+bool ffn_fp4_supported(const moe_config_t& c);
+size_t ffn_fp4_ws_bytes(const moe_config_t& c);
+cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
+                           const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                           void* ws, unsigned* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const float* out_perm, const int32_t* row_of, const float* shared, void* y,
                            bool y_bf16, int T, int d, int k, unsigned* status, int num_sms, cudaStream_t stream);
 }  // namespace moe
@@ -105,6 +110,10 @@ bool use_tc(const moe_config_t& c) {
   return !(c.flags & MOE_FLAG_SIMT_FFN) && ffn_tc_supported(c);
 }
 
+bool use_fp4(const moe_config_t& c) {
+  return !(c.flags & MOE_FLAG_SIMT_FFN) && ffn_fp4_supported(c);
+}
+
 bool use_tc_router(const moe_config_t& c) {
   return !(c.flags & MOE_FLAG_SIMT_ROUTER) && router_tc_supported(c.T, c.d_model, c.n_experts, c.x_dtype == MOE_BF16);
 }
@@ -112,6 +121,7 @@ bool use_tc_router(const moe_config_t& c) {
 size_t ffn_ws_bytes(const moe_config_t& c) {
   size_t s = ffn_simt_ws_bytes(c.T, c.top_k, c.d_ff, c.d_ff_shared);
   if (use_tc(c)) s = std::max(s, ffn_tc_ws_bytes(c));
+  if (use_fp4(c)) s = std::max(s, ffn_fp4_ws_bytes(c));
   return s;
 }
 
@@ -249,6 +259,9 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float*
   if (use_tc(*cfg))
     return cuda_status(launch_ffn_tc(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
                                      ws, di.status, di.num_sms, s));
+  if (use_fp4(*cfg))
+    return cuda_status(launch_ffn_fp4(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
+                                      ws, di.status, di.num_sms, s));
   return cuda_status(launch_ffn_simt(x, cfg->x_dtype == MOE_BF16, cfg->w_dtype, topk_w, expert_offsets,
                                      sorted_pair, weights, out_perm, shared_out, cfg->T, cfg->d_model,
                                      cfg->n_experts, cfg->top_k, cfg->d_ff, cfg->d_ff_shared, ws, di.status, s));

@@ -1,0 +1,673 @@
+// Grouped SwiGLU expert FFN on the tensor cores for NVFP4 expert weights
+// (Sarvam blog, Blackwell section: the model quantised to NVFP4; Table 1 rows
+// "Routed expert compute" / "Shared expert compute").
+//
+// NVFP4 element = e2m1 code x E4M3 block scale (16 elements along K) x fp32
+// global scale.  e2m1 x E4M3 has at most 2 + 4 significant bits and lies in
+// [2^-10, 2688], so it is exact in f16.  Converter warps therefore rebuild the
+// weight tile exactly in f16 in shared memory (cvt.rn.f16x2.e2m1x2, then one
+// f16x2 multiply by the block scale), and the MMA is tcgen05 kind::f16 with
+// f16 activations: each activation row is stored as v / s with s a power of
+// two chosen so that the row's largest magnitude lands at 2^14 -- for a bf16
+// input this is exact except for elements below amax * 2^-28.  The global
+// weight scale and the row scale (times the gate weight in the down
+// projection) are applied in the epilogue.
+//
+// Warp roles (320 threads): warp 0 issues the TMA loads of the activation
+// tiles, warp 1 owns TMEM and issues the MMAs, warps 2-5 are the epilogue,
+// warps 6-9 convert weights.  Each converter thread owns one weight row of
+// every A tile: it streams the row's packed codes and block scales with
+// cp.async several k-blocks ahead into a private ring, converts, writes the
+// swizzled f16 row, fences the async proxy and arrives on the stage's
+// "weights ready" barrier.  Every wait is bounded (timeout -> status word).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "tc_sched.cuh"
+
+namespace moe {
+
+using namespace ptx;
+
+namespace {
+
+constexpr int kF4Threads = 320;
+constexpr int kF4Epi = 128;                 // warps 2-5
+constexpr int kF4Conv = 128;                // warps 6-9
+constexpr int kF4BK = 64;                   // K elements per k-block (128 bytes of f16)
+constexpr int kF4BM = 128;                  // weight rows per tile
+constexpr uint32_t kF4ATile = kF4BM * 128;  // 16 KB f16 tile
+constexpr int kF4MaxStages = 6;
+constexpr int kF4RawSlots = 4;              // cp.async ring depth (prefetch 3 k-blocks ahead)
+constexpr int kF4RawRow = 48;               // 32 bytes of codes + 4 bytes of scales, 16-byte aligned
+constexpr uint64_t kF4WaitNs = 2000000000ull;
+constexpr uint64_t kF4DrainNs = 200000000ull;
+constexpr int kF4SmemBudget = 200 * 1024;
+
+struct F4Args {
+  const int32_t* offsets;
+  const int32_t* sorted_pair;
+  const float* topk_w;
+  const uint8_t* wq;          // routed packed codes [E][rows][K/2]
+  const uint8_t* wsc;         // routed block scales [E][rows][K/16]
+  const float* wg;            // routed global scales [E]
+  const uint8_t* sq;          // shared expert codes [rows_s][K_s/2]
+  const uint8_t* ssc;         // shared block scales
+  const float* sg;            // shared global scale (one float)
+  const float* b_scale;       // per-row activation scale [P+T]
+  __nv_bfloat16* h;           // gemm1 out [(P+T)][fmax]
+  float* out_perm;            // gemm2 out [P][d]
+  float* shared_out;          // gemm2 out [T][d]
+  int T, k, E, P, d, f, fs, fmax;
+  int TN, stages, acc_bufs, tmem_cols;
+  unsigned* status;
+};
+
+struct __align__(16) F4Ctrl {
+  uint64_t full[kF4MaxStages];     // activation tile landed (TMA tx count)
+  uint64_t aready[kF4MaxStages];   // weight tiles converted (kF4Conv arrivals)
+  uint64_t empty[kF4MaxStages];    // stage free again (MMA commit)
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint64_t ep_sync;
+  uint32_t tmem_base;
+  int abort;
+  float coef[2][kF4BM];
+  GroupTable gt;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_keep(int keep) {
+  // wait until at most `keep` groups are pending (keep is 0..3)
+  if (keep >= 3) asm volatile("cp.async.wait_group 3;" ::: "memory");
+  else if (keep == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+  else if (keep == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Four e2m1 pairs (one 32-bit word of packed codes, element 2i in the low
+// nibble of byte i) times an f16x2 block scale -> four f16x2 words.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t packed, uint32_t scale2, uint32_t (&out)[4]) {
+  asm("{\n"
+      " .reg .b8 b0, b1, b2, b3;\n"
+      " .reg .b32 h0, h1, h2, h3;\n"
+      " mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 h0, b0;\n"
+      " cvt.rn.f16x2.e2m1x2 h1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 h2, b2;\n"
+      " cvt.rn.f16x2.e2m1x2 h3, b3;\n"
+      " mul.rn.f16x2 %0, h0, %5;\n"
+      " mul.rn.f16x2 %1, h1, %5;\n"
+      " mul.rn.f16x2 %2, h2, %5;\n"
+      " mul.rn.f16x2 %3, h3, %5;\n"
+      "}\n"
+      : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+      : "r"(packed), "r"(scale2));
+}
+
+// E4M3 block-scale byte -> the same f16 value in both halves.
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t byte) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(byte | (byte << 8)), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  // D fp32 [4,6) = 1; A, B f16 (format 0); K-major; N >> 3 at 17; M >> 4 at 24
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Walks this CTA's k-block sequence (tiles blockIdx.x, +gridDim.x, ...; K/64
+// k-blocks each) -- the same order for the producer, MMA and converters.
+struct KbCursor {
+  int i, kb, nkb;
+  Tile t;
+  bool valid;
+};
+
+template <int MODE>
+__device__ __forceinline__ int tile_k(const F4Args& a, bool shr) {
+  return MODE == 1 ? a.d : (shr ? a.fs : a.f);
+}
+
+template <int MODE>
+__device__ __forceinline__ void cursor_begin(KbCursor& cu, const GroupTable& gt, int G, int total, const F4Args& a) {
+  cu.i = blockIdx.x;
+  cu.kb = 0;
+  cu.valid = cu.i < total;
+  if (cu.valid) {
+    cu.t = decode_tile(gt, G, cu.i, a.TN);
+    cu.nkb = tile_k<MODE>(a, cu.t.g == a.E) / kF4BK;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void cursor_next(KbCursor& cu, const GroupTable& gt, int G, int total, const F4Args& a) {
+  if (!cu.valid) return;
+  if (++cu.kb < cu.nkb) return;
+  cu.kb = 0;
+  cu.i += gridDim.x;
+  cu.valid = cu.i < total;
+  if (cu.valid) {
+    cu.t = decode_tile(gt, G, cu.i, a.TN);
+    cu.nkb = tile_k<MODE>(a, cu.t.g == a.E) / kF4BK;
+  }
+}
+
+// Global row of weight tile `a_idx` (0 = gate / down, 1 = up) for this tile.
+template <int MODE>
+__device__ __forceinline__ void weight_row(const F4Args& a, const Tile& t, int a_idx, int r, const uint8_t** q,
+                                           const uint8_t** sc, int* K) {
+  const bool shr = t.g == a.E;
+  int row;
+  if (MODE == 1) {
+    const int width = shr ? a.fs : a.f;
+    row = (shr ? 0 : t.g * 2 * a.f) + (a_idx ? width : 0) + t.wt * kF4BM + r;
+    *K = a.d;
+  } else {
+    row = (shr ? 0 : t.g * a.d) + t.wt * kF4BM + r;
+    *K = shr ? a.fs : a.f;
+  }
+  *q = (shr ? a.sq : a.wq) + static_cast<size_t>(row) * (*K / 2);
+  *sc = (shr ? a.ssc : a.wsc) + static_cast<size_t>(row) * (*K / 16);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kF4Threads, 1)
+ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
+  constexpr int NA = (MODE == 1) ? 2 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int N = a.TN;                                   // one f16 column per token
+  const uint32_t b_bytes = static_cast<uint32_t>(N) * 128;
+  const uint32_t stage_bytes = NA * kF4ATile + ((b_bytes + 1023u) & ~1023u);
+  uint8_t* raw = smem + a.stages * stage_bytes;         // [slots][NA][128 rows][48 B]
+  F4Ctrl* c = reinterpret_cast<F4Ctrl*>(raw + kF4RawSlots * NA * kF4BM * kF4RawRow);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.E + 1;
+  volatile int* abort = &c->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_u32(&c->full[s]), 1);
+      mbar_init(smem_u32(&c->aready[s]), kF4Conv);
+      mbar_init(smem_u32(&c->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&c->tfull[b]), 1);
+      mbar_init(smem_u32(&c->tempty[b]), kF4Epi);
+    }
+    mbar_init(smem_u32(&c->drain), 1);
+    mbar_init(smem_u32(&c->ep_sync), kF4Epi);
+    c->abort = 0;
+    fence_barrier_init();
+    if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kF4BM, a.fs / kF4BM, a.status);
+    else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kF4BM, a.d / kF4BM, a.status);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c->tmem_base;
+  const int total = c->gt.tile_start[G];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer (activations)
+      tma_prefetch_desc(&mapB);
+      int st = 0;
+      uint32_t ph = 0, pending = 0, last_par = 0;
+      KbCursor cu;
+      cursor_begin<MODE>(cu, c->gt, G, total, a);
+      for (; cu.valid && !*abort; cursor_next<MODE>(cu, c->gt, G, total, a)) {
+        if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, kF4WaitNs)) break;
+        const uint32_t full = smem_u32(&c->full[st]);
+        mbar_arrive_expect_tx(full, b_bytes);
+        tma_load_2d(smem_u32(smem + st * stage_bytes + NA * kF4ATile), &mapB, cu.kb * kF4BK, cu.t.row0, full);
+        pending |= 1u << st;
+        last_par = (last_par & ~(1u << st)) | (ph << st);
+        if (++st == a.stages) {
+          st = 0;
+          ph ^= 1u;
+        }
+      }
+      int no_abort = 0;
+      for (int s = 0; s < a.stages; ++s)
+        if (pending & (1u << s)) mbar_wait(smem_u32(&c->full[s]), (last_par >> s) & 1u, &no_abort, kF4DrainNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_f16(kF4BM, N);
+      int st = 0, ab = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+        const Tile t = decode_tile(c->gt, G, i, a.TN);
+        const int nkb = tile_k<MODE>(a, t.g == a.E) / kF4BK;
+        if (!mbar_wait(smem_u32(&c->tempty[ab]), aph ^ 1u, abort, kF4WaitNs)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem + static_cast<uint32_t>(ab * NA * N);
+        const uint32_t d1 = d0 + static_cast<uint32_t>(N);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(smem_u32(&c->full[st]), ph, abort, kF4WaitNs) ||
+              !mbar_wait(smem_u32(&c->aready[st]), ph, abort, kF4WaitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + st * stage_bytes);
+          const uint64_t da0 = desc_sw128(sA);
+          const uint64_t da1 = desc_sw128(sA + kF4ATile);
+          const uint64_t db = desc_sw128(sA + NA * kF4ATile);
+#pragma unroll
+          for (int kk = 0; kk < kF4BK / 16; ++kk) {
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            mma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
+            if (MODE == 1) mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+          }
+          mma_commit(smem_u32(&c->empty[st]));
+          if (++st == a.stages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&c->tfull[ab]));
+        if (++ab == a.acc_bufs) {
+          ab = 0;
+          aph ^= 1u;
+        }
+      }
+      mma_commit(smem_u32(&c->drain));
+      int no_abort = 0;
+      mbar_wait(smem_u32(&c->drain), 0, &no_abort, kF4DrainNs);
+    }
+  } else if (warp < 6) {
+    // -------------------------------------------------- epilogue (warps 2..5)
+    const int sub = warp & 3;
+    const int n = sub * 32 + lane;
+    const int et = threadIdx.x - 64;                 // 0..127
+    const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
+    int ab = 0, cb_par = 0;
+    uint32_t aph = 0, eph = 0;
+    for (int i = blockIdx.x; i < total; i += gridDim.x) {
+      const Tile t = decode_tile(c->gt, G, i, a.TN);
+      const bool shr = t.g == a.E;
+      {
+        float cf = 0.f;
+        if (et < t.nrows) {
+          const int row = t.row0 + et;
+          cf = a.b_scale[row] * (shr ? a.sg[0] : a.wg[t.g]);
+          if (MODE == 2 && !shr) {
+            const int p = a.sorted_pair[row];
+            if (p >= 0 && p < a.P) {
+              cf *= a.topk_w[p];
+            } else {
+              cf = 0.f;
+              set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
+            }
+          }
+        }
+        c->coef[cb_par][et] = cf;
+      }
+      mbar_arrive(smem_u32(&c->ep_sync));
+      if (!mbar_wait(smem_u32(&c->ep_sync), eph, abort, kF4WaitNs)) break;
+      eph ^= 1u;
+      const float* coef = c->coef[cb_par];
+      cb_par ^= 1;
+      if (!mbar_wait(smem_u32(&c->tfull[ab]), aph, abort, kF4WaitNs)) break;
+      tc_fence_after();
+      const int col = t.wt * kF4BM + n;
+      if (MODE == 1) {
+        const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
+        for (int c0 = 0; c0 < N; c0 += 32) {       // 32 tokens per chunk
+          float gv[32], uv[32], cf[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) cf[jj] = coef[(c0 + jj) & (kF4BM - 1)];
+          tmem_ld32x2(cb + c0, cb + N + c0, gv, uv);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = c0 + jj;
+            if (j < t.nrows) {
+              const float g = gv[jj] * cf[jj];
+              const float u = uv[jj] * cf[jj];
+              a.h[static_cast<size_t>(t.row0 + j) * a.fmax + col] = __float2bfloat16_rn(silu(g) * u);
+            }
+          }
+        }
+      } else {
+        const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
+        float* outb = shr ? a.shared_out + (static_cast<size_t>(t.row0 - a.P) * a.d + col)
+                          : a.out_perm + (static_cast<size_t>(t.row0) * a.d + col);
+        for (int c0 = 0; c0 < N; c0 += 64) {       // 64 tokens per chunk
+          float d0[32], d1[32];
+          tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
+#pragma unroll
+          for (int jj = 0; jj < 64; ++jj) {
+            const int j = c0 + jj;
+            if (j < t.nrows) {
+              const float v = jj < 32 ? d0[jj] : d1[jj - 32];
+              outb[static_cast<size_t>(j) * a.d] = v * coef[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&c->tempty[ab]));
+      if (++ab == a.acc_bufs) {
+        ab = 0;
+        aph ^= 1u;
+      }
+    }
+  } else {
+    // -------------------------------------------------- weight converters (warps 6..9)
+    const int r = threadIdx.x - 192;                  // weight row within the tile, 0..127
+    const uint32_t raw_base = smem_u32(raw);
+    const uint32_t raw_slot_bytes = NA * kF4BM * kF4RawRow;
+    KbCursor fetch, conv;
+    cursor_begin<MODE>(fetch, c->gt, G, total, a);
+    cursor_begin<MODE>(conv, c->gt, G, total, a);
+    // prologue: k-blocks 0 .. kF4RawSlots-2 in flight
+    int issued = 0;
+    for (; issued < kF4RawSlots - 1; ++issued) {
+      if (fetch.valid) {
+        const uint32_t slot = raw_base + (issued % kF4RawSlots) * raw_slot_bytes;
+        for (int ai = 0; ai < NA; ++ai) {
+          const uint8_t *q, *sc;
+          int K;
+          weight_row<MODE>(a, fetch.t, ai, r, &q, &sc, &K);
+          const uint32_t dst = slot + (ai * kF4BM + r) * kF4RawRow;
+          cp_async16(dst, q + fetch.kb * 32);
+          cp_async16(dst + 16, q + fetch.kb * 32 + 16);
+          cp_async4(dst + 32, sc + fetch.kb * 4);
+        }
+        cursor_next<MODE>(fetch, c->gt, G, total, a);
+      }
+      cp_commit();
+    }
+    int st = 0, q_idx = 0;
+    uint32_t ph = 0;
+    for (; conv.valid && !*abort; cursor_next<MODE>(conv, c->gt, G, total, a), ++q_idx) {
+      // keep the ring full: issue k-block q_idx + slots - 1
+      if (fetch.valid) {
+        const uint32_t slot = raw_base + (issued % kF4RawSlots) * raw_slot_bytes;
+        for (int ai = 0; ai < NA; ++ai) {
+          const uint8_t *q, *sc;
+          int K;
+          weight_row<MODE>(a, fetch.t, ai, r, &q, &sc, &K);
+          const uint32_t dst = slot + (ai * kF4BM + r) * kF4RawRow;
+          cp_async16(dst, q + fetch.kb * 32);
+          cp_async16(dst + 16, q + fetch.kb * 32 + 16);
+          cp_async4(dst + 32, sc + fetch.kb * 4);
+        }
+        cursor_next<MODE>(fetch, c->gt, G, total, a);
+      }
+      cp_commit();
+      ++issued;
+      cp_wait_keep(kF4RawSlots - 1);                    // this k-block's raw row has landed
+      if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, kF4WaitNs)) break;
+      const uint8_t* rslot = raw + (q_idx % kF4RawSlots) * raw_slot_bytes;
+      for (int ai = 0; ai < NA; ++ai) {
+        const uint8_t* src = rslot + (ai * kF4BM + r) * kF4RawRow;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(src);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(src + 16);
+        const uint32_t scw = *reinterpret_cast<const uint32_t*>(src + 32);
+        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint8_t* dst_row = smem + st * stage_bytes + ai * kF4ATile + r * 128;
+#pragma unroll
+        for (int chunk = 0; chunk < 8; ++chunk) {     // 8 elements (16 bytes of f16) per chunk
+          const uint32_t s2 = e4m3_to_f16x2_bcast((scw >> (8 * (chunk >> 1))) & 0xffu);
+          uint32_t hv[4];
+          e2m1x8_to_f16(words[chunk], s2, hv);
+          *reinterpret_cast<uint4*>(dst_row + ((chunk ^ (r & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(smem_u32(&c->aready[st]));
+      if (++st == a.stages) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+  if (threadIdx.x == 0 && c->abort) set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+}
+
+// Row scaler: f16 copy of an activation row divided by s = 2^(e-14), where
+// amax = m 2^e (m in [0.5,1)), so the row's largest magnitude is m 2^14.
+// One warp per row of the (P+T)-row space; GATHER_X takes row r < P from
+// x[sorted_pair[r]/k] and row P+t from x[t], else row r of H (width f for
+// routed rows, f_s for shared rows).
+template <bool GATHER_X>
+__global__ void __launch_bounds__(256)
+scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
+                    int width_r, int width_s, int src_stride, __half* __restrict__ dst, int dst_stride,
+                    float* __restrict__ scale, unsigned* status) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= P + T) return;
+  __half* drow = dst + static_cast<size_t>(row) * dst_stride;
+  const uint16_t* s;
+  int width;
+  if (GATHER_X) {
+    int t = row - P;
+    width = width_r;
+    if (row < P) {
+      const int p = sorted_pair[row];
+      t = (p >= 0 && p < P) ? p / k : -1;
+    }
+    if (t < 0) {
+      if (lane == 0) set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      for (int c = lane * 8; c < width; c += 256) *reinterpret_cast<uint4*>(drow + c) = make_uint4(0, 0, 0, 0);
+      if (lane == 0) scale[row] = 1.f;
+      return;
+    }
+    s = src + static_cast<size_t>(t) * src_stride;
+  } else {
+    s = src + static_cast<size_t>(row) * src_stride;
+    width = row < P ? width_r : width_s;
+  }
+  float amax = 0.f;
+  for (int c = lane * 8; c < width; c += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  float sc = 1.f;
+  if (amax > 0.f && isfinite(amax)) {
+    int e;
+    frexpf(amax, &e);
+    sc = ldexpf(1.0f, e - 14);
+  }
+  const float inv = 1.0f / sc;   // exact: a power of two
+  for (int c = lane * 8; c < width; c += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * inv, __uint_as_float(w[i] & 0xffff0000u) * inv);
+      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(drow + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (lane == 0) scale[row] = sc;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn f4_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// f16 matrix [rows][cols] (pitch `pitch` elements), box 64 elements x box_rows, 128-byte swizzle.
+bool make_f16_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch, uint32_t box_rows) {
+  EncodeTiledFn fn = f4_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kF4BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct F4Plan {
+  size_t xh, sx, h, hh, sh, total;
+  int TN;
+};
+
+F4Plan f4_plan(const moe_config_t& c) {
+  const size_t P = static_cast<size_t>(c.T) * c.top_k, R = P + c.T;
+  const size_t fmax = std::max(c.d_ff, c.d_ff_shared);
+  F4Plan p;
+  size_t o = 0;
+  auto take = [&](size_t b) { size_t at = o; o += align_up(b, 1024); return at; };
+  p.xh = take(2 * R * c.d_model);
+  p.sx = take(4 * R);
+  p.h = take(2 * R * fmax);
+  p.hh = take(2 * R * fmax);
+  p.sh = take(4 * R);
+  p.total = o;
+  const double avg = static_cast<double>(P) / c.n_experts;
+  p.TN = avg <= 12 ? 16 : avg <= 24 ? 32 : avg <= 48 ? 64 : 128;
+  return p;
+}
+
+template <int MODE>
+cudaError_t launch_f4_gemm(const CUtensorMap& mB, F4Args a, int wtiles_max, int num_sms, cudaStream_t stream) {
+  constexpr int NA = (MODE == 1) ? 2 : 1;
+  const int N = a.TN;
+  const int stage_bytes = NA * kF4ATile + align_up(static_cast<size_t>(N) * 128, 1024);
+  const int raw_bytes = kF4RawSlots * NA * kF4BM * kF4RawRow;
+  a.stages = std::min(kF4MaxStages, (kF4SmemBudget - raw_bytes) / stage_bytes);
+  const int per_acc = NA * N;
+  a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
+  // epilogue loads: gemm1 32 columns at c0 and N + c0; gemm2 64 columns at c0
+  const int last = (a.acc_bufs - 1) * per_acc;
+  const int reach = (MODE == 1) ? last + N + (N + 31) / 32 * 32 : last + (N + 63) / 64 * 64;
+  int cols = 32;
+  while (cols < reach) cols *= 2;
+  if (cols > 512 || a.stages < 2) return cudaErrorInvalidConfiguration;
+  a.tmem_cols = cols;
+  size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + raw_bytes + sizeof(F4Ctrl);
+  smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
+  cudaError_t err = cudaFuncSetAttribute(ffn_fp4_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const long long tiles_ub =
+      static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
+  count_launches(1);
+  ffn_fp4_kernel<MODE><<<grid, kF4Threads, smem, stream>>>(mB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool ffn_fp4_supported(const moe_config_t& c) {
+  return c.w_dtype == MOE_NVFP4 && c.x_dtype == MOE_BF16 && c.d_ff % 128 == 0 && c.d_ff_shared % 128 == 0 &&
+         c.d_model % 128 == 0 && f4_encode_fn() != nullptr;
+}
+
+size_t ffn_fp4_ws_bytes(const moe_config_t& c) { return f4_plan(c).total; }
+
+cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
+                           const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                           void* ws, unsigned* status, int num_sms, cudaStream_t stream) {
+  const int T = c.T, k = c.top_k, E = c.n_experts, d = c.d_model, f = c.d_ff, fs = c.d_ff_shared;
+  if (T == 0) return cudaSuccess;
+  const int P = T * k, R = P + T;
+  const int fmax = std::max(f, fs);
+  const F4Plan pl = f4_plan(c);
+  char* base = static_cast<char*>(ws);
+  __half* xh = reinterpret_cast<__half*>(base + pl.xh);
+  float* sx = reinterpret_cast<float*>(base + pl.sx);
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(base + pl.h);
+  __half* hh = reinterpret_cast<__half*>(base + pl.hh);
+  float* sh = reinterpret_cast<float*>(base + pl.sh);
+
+  const int qblocks = ceil_div(R, 8);
+  count_launches(1);
+  scale16_rows_kernel<true><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d,
+                                                         d, d, xh, d, sx, status);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  F4Args a = {};
+  a.offsets = offsets; a.sorted_pair = sorted_pair; a.topk_w = topk_w;
+  a.h = h; a.out_perm = out_perm; a.shared_out = shared_out;
+  a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
+  a.TN = pl.TN; a.status = status;
+
+  CUtensorMap mB;
+  // gemm1: gate / up
+  if (!make_f16_map(&mB, xh, R, d, d, pl.TN)) return cudaErrorInvalidValue;
+  a.wq = static_cast<const uint8_t*>(w->w13); a.wsc = static_cast<const uint8_t*>(w->w13_scale); a.wg = w->w13_gscale;
+  a.sq = static_cast<const uint8_t*>(w->s13); a.ssc = static_cast<const uint8_t*>(w->s13_scale); a.sg = w->s13_gscale;
+  a.b_scale = sx;
+  err = launch_f4_gemm<1>(mB, a, fmax / kF4BM, num_sms, stream);
+  if (err != cudaSuccess) return err;
+
+  count_launches(1);
+  scale16_rows_kernel<false><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P, T, k, f,
+                                                          fs, fmax, hh, fmax, sh, status);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  // gemm2: down projection, gate weight, outputs
+  if (!make_f16_map(&mB, hh, R, fmax, fmax, pl.TN)) return cudaErrorInvalidValue;
+  a.wq = static_cast<const uint8_t*>(w->w2); a.wsc = static_cast<const uint8_t*>(w->w2_scale); a.wg = w->w2_gscale;
+  a.sq = static_cast<const uint8_t*>(w->s2); a.ssc = static_cast<const uint8_t*>(w->s2_scale); a.sg = w->s2_gscale;
+  a.b_scale = sh;
+  return launch_f4_gemm<2>(mB, a, d / kF4BM, num_sms, stream);
+}
+
+}  // namespace moe

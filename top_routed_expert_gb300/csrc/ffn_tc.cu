@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tc_sched.cuh"
 
 namespace moe {
 
@@ -72,13 +73,6 @@ struct TcArgs {
   unsigned* status;
 };
 
-struct GroupTable {
-  int tile_start[kMaxGroups + 1];
-  int row_base[kMaxGroups];    // first row of the group in the (P+T)-row activation space
-  int rows[kMaxGroups];
-  int mtiles[kMaxGroups];
-};
-
 struct __align__(16) TcCtrl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
@@ -91,22 +85,6 @@ struct __align__(16) TcCtrl {
   float coef[2][kBM];          // per-row epilogue coefficient, double-buffered by tile parity
   GroupTable gt;
 };
-
-struct Tile {
-  int g, wt, row0, nrows;
-};
-
-__device__ __forceinline__ Tile decode_tile(const GroupTable& gt, int G, int i, int TN) {
-  Tile t;
-  t.g = find_group(gt.tile_start, G, i);
-  const int local = i - gt.tile_start[t.g];
-  const int mt_n = gt.mtiles[t.g];
-  t.wt = local / mt_n;
-  const int mt = local - t.wt * mt_n;
-  t.row0 = gt.row_base[t.g] + mt * TN;
-  t.nrows = min(TN, gt.rows[t.g] - mt * TN);
-  return t;
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -137,30 +115,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     c->abort = 0;
     fence_barrier_init();
     // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
-    int acc = 0;
-    for (int g = 0; g < G; ++g) {
-      int base, rows;
-      if (g < a.E) {
-        base = a.offsets[g];
-        rows = a.offsets[g + 1] - base;
-        if (base < 0 || rows < 0 || base + rows > a.P) {
-          set_status(a.status, MOE_ERR_DEVICE_BOUNDS);
-          base = 0;
-          rows = 0;
-        }
-      } else {
-        base = a.P;
-        rows = a.T;
-      }
-      const int wt = (MODE == 1) ? ((g < a.E ? a.f : a.fs) / kBM) : (a.d / kBM);
-      const int mt = (rows + a.TN - 1) / a.TN;
-      c->gt.tile_start[g] = acc;
-      c->gt.row_base[g] = base;
-      c->gt.rows[g] = rows;
-      c->gt.mtiles[g] = mt;
-      acc += mt * wt;
-    }
-    c->gt.tile_start[G] = acc;
+    if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kBM, a.fs / kBM, a.status);
+    else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kBM, a.d / kBM, a.status);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
