@@ -265,8 +265,9 @@ def measure(layer, x, cfg, steps, warmup, world, dev, gpu_index, abi, torch, clo
     offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
     sp = torch.empty(P, dtype=torch.int32, device=dev)
     row_of = torch.empty(P, dtype=torch.int32, device=dev)
-    out_perm = torch.empty((P, d), dtype=torch.float32, device=dev)
-    shared = torch.empty((T, d), dtype=torch.float32, device=dev)
+    edt = torch.bfloat16 if (layer.flags & abi.MOE_FLAG_BF16_EXPERT_OUT) else torch.float32
+    out_perm = torch.empty((P, d), dtype=edt, device=dev)
+    shared = torch.empty((T, d), dtype=edt, device=dev)
     y = torch.empty((T, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -355,7 +356,8 @@ def run_ours(args, world, rank, local):
     moe.build()
     inp = moe_synth.make_inputs(args.workload)
     cfg = inp.cfg
-    layer = MoELayer(inp, device=dev, flags=abi.MOE_FLAG_SIMT_FFN if args.simt else 0)
+    flags = (abi.MOE_FLAG_SIMT_FFN if args.simt else 0) | (abi.MOE_FLAG_BF16_EXPERT_OUT if args.bf16_expert_out else 0)
+    layer = MoELayer(inp, device=dev, flags=flags)
     x = _to_dev(inp.x, dev)
     T, d = cfg.T, cfg.d
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
@@ -419,6 +421,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD_TEXT[args.workload], "T": T, "d_model": d, "n_experts": cfg.E,
                    "top_k": cfg.k, "d_ff": cfg.f, "d_ff_shared": cfg.fs, "weights": cfg.w_dtype,
                    "ffn_path": "simt" if args.simt else "default",
+                   "expert_out": "bf16" if args.bf16_expert_out else "fp32",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: expert weights %.2f GB per pass" % (m["alg"]["ffn_bytes"] / 1e9)},
         "stages_ms": m["stage_ms"],
@@ -443,6 +446,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="decode")
     ap.add_argument("--simt", action="store_true", help="force the CUDA-core expert kernels")
+    ap.add_argument("--bf16-expert-out", action="store_true",
+                    help="store the expert outputs in bf16 (MOE_FLAG_BF16_EXPERT_OUT)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the T=8192 point of the decode run")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")

@@ -62,6 +62,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtyp
 /* Flags (moe_config_t.flags). */
 #define MOE_FLAG_SIMT_FFN 0x1u     /* run the expert FFN on the CUDA-core kernels */
 #define MOE_FLAG_SIMT_ROUTER 0x2u  /* run the router on the CUDA-core kernel       */
+#define MOE_FLAG_BF16_EXPERT_OUT 0x4u  /* out_perm / shared_out in bf16 (default fp32) */
 
 typedef struct {
   int32_t T;            /* tokens, >= 0 (0 is a no-op)                          */
@@ -189,22 +190,27 @@ moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_id
  *   x              [T][d] (cfg->x_dtype)
  *   topk_w         [T][k] float gates (from moe_route)
  *   expert_offsets [E+1], sorted_pair [T*k] (from moe_permute)
- *   out_perm       [T*k][d] float out: row r = topk_w[p] * FFN_e(x[t]) for
+ *   out_perm       [T*k][d] out: row r = topk_w[p] * FFN_e(x[t]) for
  *                  p = sorted_pair[r] = t*k+j routed to expert e
- *   shared_out     [T][d] float out: FFN_shared(x[t])
+ *   shared_out     [T][d] out: FFN_shared(x[t])
+ * out_perm and shared_out are fp32, or bf16 with MOE_FLAG_BF16_EXPERT_OUT
+ * (half the bytes; each expert output is then rounded once to bf16, which
+ * costs about 1e-3 relative error in y; all sums stay fp32).
  */
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float* topk_w,
                             const int32_t* expert_offsets, const int32_t* sorted_pair,
-                            const moe_weights_t* weights, float* out_perm, float* shared_out,
+                            const moe_weights_t* weights, void* out_perm, void* shared_out,
                             void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * Deterministic combine: y[t] = shared_out[t] + sum_{j=0..k-1} out_perm[row_of[t*k+j]],
  * added in slot order j (Sarvam summary section 2.1: shared plus routed
- * experts).  y is [T][d] in cfg->y_dtype.  Uses no workspace.
+ * experts).  out_perm / shared_out as written by moe_expert_ffn (fp32, or
+ * bf16 with MOE_FLAG_BF16_EXPERT_OUT); the sum is taken in fp32.  y is [T][d]
+ * in cfg->y_dtype.  Uses no workspace.
  */
-moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const int32_t* row_of,
-                         const float* shared_out, void* y, moe_stream_t stream);
+moe_status_t moe_combine(const moe_config_t* cfg, const void* out_perm, const int32_t* row_of,
+                         const void* shared_out, void* y, moe_stream_t stream);
 
 /*
  * The whole layer: route -> permute -> expert FFN (+ shared) -> combine, all

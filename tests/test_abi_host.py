@@ -54,7 +54,7 @@ def cfg(**kw):
     dict(T=-1), dict(d_model=100), dict(d_model=0), dict(d_model=32768), dict(n_experts=0),
     dict(n_experts=300), dict(top_k=0), dict(top_k=17), dict(n_experts=4, top_k=5), dict(d_ff=100),
     dict(d_ff_shared=0), dict(x_dtype=abi.MOE_E4M3), dict(w_dtype=abi.MOE_BF16), dict(y_dtype=abi.MOE_NVFP4),
-    dict(flags=0x80), dict(flags=0x4),
+    dict(flags=0x80), dict(flags=0x8),
 ])
 def test_invalid_config_rejected(lib, bad):
     c = cfg(**bad)

@@ -21,20 +21,20 @@ cudaError_t launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, i
                            int32_t* row_of, void* ws, unsigned* status, cudaStream_t stream);
 size_t ffn_simt_ws_bytes(int T, int k, int f, int fs);
 cudaError_t launch_ffn_simt(const void* x, bool x_bf16, int w_dtype, const float* topk_w, const int32_t* offsets,
-                            const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
-                            int T, int d, int E, int k, int f, int fs, void* ws, unsigned* status,
+                            const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
+                            bool out_bf16, int T, int d, int E, int k, int f, int fs, void* ws, unsigned* status,
                             cudaStream_t stream);
 bool ffn_tc_supported(const moe_config_t& c);
 size_t ffn_tc_ws_bytes(const moe_config_t& c);
 cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
-                          const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                          const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
                           void* ws, unsigned* status, int num_sms, cudaStream_t stream);
 bool ffn_fp4_supported(const moe_config_t& c);
 size_t ffn_fp4_ws_bytes(const moe_config_t& c);
 cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
-                           const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                           const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
                            void* ws, unsigned* status, int num_sms, cudaStream_t stream);
-cudaError_t launch_combine(const float* out_perm, const int32_t* row_of, const float* shared, void* y,
+cudaError_t launch_combine(const void* out_perm, const int32_t* row_of, const void* shared, void* y, bool in_bf16,
                            bool y_bf16, int T, int d, int k, unsigned* status, int num_sms, cudaStream_t stream);
 }  // namespace moe
 
@@ -102,7 +102,8 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_E4M3 && c->w_dtype != MOE_NVFP4) return MOE_ERR_INVALID_ARG;
   if (c->y_dtype != MOE_F32 && c->y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(c->T) * c->top_k > (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER)) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER | MOE_FLAG_BF16_EXPERT_OUT)) != 0)
+    return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -140,8 +141,9 @@ FwdPlan plan_forward(const moe_config_t& c) {
   p.offsets = take(sizeof(int32_t) * (c.n_experts + 1));
   p.sorted_pair = take(sizeof(int32_t) * P);
   p.row_of = take(sizeof(int32_t) * P);
-  p.out_perm = take(sizeof(float) * P * c.d_model);
-  p.shared_out = take(sizeof(float) * static_cast<size_t>(c.T) * c.d_model);
+  const size_t esz = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) ? 2 : 4;   // expert-output element size
+  p.out_perm = take(esz * P * c.d_model);
+  p.shared_out = take(esz * static_cast<size_t>(c.T) * c.d_model);
   size_t scratch = std::max(permute_ws_bytes(static_cast<int>(P), c.n_experts), ffn_ws_bytes(c));
   if (use_tc_router(c)) scratch = std::max(scratch, router_tc_ws_bytes(c.d_model));
   p.scratch = take(scratch);
@@ -244,7 +246,7 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32
 
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float* topk_w,
                             const int32_t* expert_offsets, const int32_t* sorted_pair, const moe_weights_t* weights,
-                            float* out_perm, float* shared_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                            void* out_perm, void* shared_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
   if (cfg->T == 0) return MOE_OK;
@@ -263,12 +265,13 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float*
     return cuda_status(launch_ffn_fp4(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
                                       ws, di.status, di.num_sms, s));
   return cuda_status(launch_ffn_simt(x, cfg->x_dtype == MOE_BF16, cfg->w_dtype, topk_w, expert_offsets,
-                                     sorted_pair, weights, out_perm, shared_out, cfg->T, cfg->d_model,
+                                     sorted_pair, weights, out_perm, shared_out,
+                                     (cfg->flags & MOE_FLAG_BF16_EXPERT_OUT) != 0, cfg->T, cfg->d_model,
                                      cfg->n_experts, cfg->top_k, cfg->d_ff, cfg->d_ff_shared, ws, di.status, s));
 }
 
-moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const int32_t* row_of,
-                         const float* shared_out, void* y, moe_stream_t stream) {
+moe_status_t moe_combine(const moe_config_t* cfg, const void* out_perm, const int32_t* row_of,
+                         const void* shared_out, void* y, moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
   if (cfg->T == 0) return MOE_OK;
@@ -276,7 +279,8 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* out_perm, const i
   if (!aligned(out_perm, 16) || !aligned(shared_out, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
   DeviceInfo di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  return cuda_status(launch_combine(out_perm, row_of, shared_out, y, cfg->y_dtype == MOE_BF16, cfg->T,
+  return cuda_status(launch_combine(out_perm, row_of, shared_out, y, (cfg->flags & MOE_FLAG_BF16_EXPERT_OUT) != 0,
+                                    cfg->y_dtype == MOE_BF16, cfg->T,
                                     cfg->d_model, cfg->top_k, di.status, di.num_sms,
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -307,8 +311,8 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const flo
   int32_t* offsets = reinterpret_cast<int32_t*>(base + p.offsets);
   int32_t* sorted_pair = reinterpret_cast<int32_t*>(base + p.sorted_pair);
   int32_t* row_of = reinterpret_cast<int32_t*>(base + p.row_of);
-  float* out_perm = reinterpret_cast<float*>(base + p.out_perm);
-  float* shared_out = reinterpret_cast<float*>(base + p.shared_out);
+  void* out_perm = base + p.out_perm;
+  void* shared_out = base + p.shared_out;
   void* scratch = base + p.scratch;
   const size_t scratch_bytes = p.total - p.scratch;
   if ((st = moe_route(cfg, x, w_router, expert_bias, ids, w, scratch, scratch_bytes, stream)) != MOE_OK) return st;

@@ -3,6 +3,10 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <set>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -13,10 +17,39 @@
 namespace moe {
 
 constexpr int kMaxExperts = 256;
+constexpr int kMaxGroups = kMaxExperts + 1;   // routed experts + the shared expert
 
 // Host-side count of kernel launches (moe_launch_count); defined in api.cu.
 void count_launches(int n);
-constexpr int kMaxGroups = kMaxExperts + 1;   // routed experts + the shared expert
+
+// Raises a kernel's dynamic shared-memory limit to at least smem_bytes (and,
+// optionally, allows non-portable cluster sizes).  The limit is one value per
+// (kernel, device), so it is only ever raised -- lowering it would break a
+// later launch that needs more -- and the attribute call is made only when the
+// limit actually grows: setting function attributes on every launch costs far
+// more than the launch.
+inline cudaError_t ensure_kernel_attrs(const void* kernel, int smem_bytes, bool nonportable_cluster = false) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> smem_limit;
+  static std::set<std::pair<const void*, int>> nonportable;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const auto key = std::make_pair(kernel, dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = smem_limit.find(key);
+  if (it == smem_limit.end() || it->second < smem_bytes) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (err != cudaSuccess) return err;
+    smem_limit[key] = smem_bytes;
+  }
+  if (nonportable_cluster && !nonportable.count(key)) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) return err;
+    nonportable.insert(key);
+  }
+  return cudaSuccess;
+}
 
 // Device status word: kernels record the first fault they see with
 // atomicCAS(0 -> code) and carry on with the fault contained (skip the bad
@@ -50,6 +83,12 @@ __device__ __forceinline__ float e2m1_to_float(uint32_t code) {
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+// Expert-output element store: bf16 (default) or fp32.
+__device__ __forceinline__ void store_out(void* base, size_t idx, float v, bool out_bf16) {
+  if (out_bf16) static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
+  else static_cast<float*>(base)[idx] = v;
+}
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ __forceinline__ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

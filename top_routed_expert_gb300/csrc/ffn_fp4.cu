@@ -57,8 +57,9 @@ struct F4Args {
   const float* sg;            // shared global scale (one float)
   const float* b_scale;       // per-row activation scale [P+T]
   __nv_bfloat16* h;           // gemm1 out [(P+T)][fmax]
-  float* out_perm;            // gemm2 out [P][d]
-  float* shared_out;          // gemm2 out [T][d]
+  void* out_perm;             // gemm2 out [P][d] bf16 or fp32
+  void* shared_out;           // gemm2 out [T][d]
+  bool out_bf16;
   int T, k, E, P, d, f, fs, fmax;
   int TN, stages, acc_bufs, tmem_cols;
   unsigned* status;
@@ -220,9 +221,9 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
     mbar_init(smem_u32(&c->ep_sync), kF4Epi);
     c->abort = 0;
     fence_barrier_init();
-    if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kF4BM, a.fs / kF4BM, a.status);
-    else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kF4BM, a.d / kF4BM, a.status);
   }
+  if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kF4BM, a.fs / kF4BM, a.status);
+  else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kF4BM, a.d / kF4BM, a.status);
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
     tmem_relinquish();
@@ -360,8 +361,8 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
         }
       } else {
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
-        float* outb = shr ? a.shared_out + (static_cast<size_t>(t.row0 - a.P) * a.d + col)
-                          : a.out_perm + (static_cast<size_t>(t.row0) * a.d + col);
+        void* outp = shr ? a.shared_out : a.out_perm;
+        const size_t out0 = static_cast<size_t>(shr ? t.row0 - a.P : t.row0) * a.d + col;
         for (int c0 = 0; c0 < N; c0 += 64) {       // 64 tokens per chunk
           float d0[32], d1[32];
           tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
@@ -370,7 +371,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
             const int j = c0 + jj;
             if (j < t.nrows) {
               const float v = jj < 32 ? d0[jj] : d1[jj - 32];
-              outb[static_cast<size_t>(j) * a.d] = v * coef[j];
+              store_out(outp, out0 + static_cast<size_t>(j) * a.d, v * coef[j], a.out_bf16);
             }
           }
         }
@@ -599,8 +600,7 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, F4Args a, int wtiles_max, int 
   a.tmem_cols = cols;
   size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + raw_bytes + sizeof(F4Ctrl);
   smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
-  cudaError_t err = cudaFuncSetAttribute(ffn_fp4_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_fp4_kernel<MODE>), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const long long tiles_ub =
       static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
@@ -620,7 +620,7 @@ bool ffn_fp4_supported(const moe_config_t& c) {
 size_t ffn_fp4_ws_bytes(const moe_config_t& c) { return f4_plan(c).total; }
 
 cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
-                           const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                           const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
                            void* ws, unsigned* status, int num_sms, cudaStream_t stream) {
   const int T = c.T, k = c.top_k, E = c.n_experts, d = c.d_model, f = c.d_ff, fs = c.d_ff_shared;
   if (T == 0) return cudaSuccess;
@@ -644,6 +644,7 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   F4Args a = {};
   a.offsets = offsets; a.sorted_pair = sorted_pair; a.topk_w = topk_w;
   a.h = h; a.out_perm = out_perm; a.shared_out = shared_out;
+  a.out_bf16 = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0;
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
   a.TN = pl.TN; a.status = status;
 

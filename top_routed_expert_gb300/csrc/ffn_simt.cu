@@ -87,8 +87,9 @@ struct FfnArgs {
   moe_weights_t w;
   float* h;                   // [P][f]   routed SwiGLU activations
   float* hs;                  // [T][fs]  shared-expert activations
-  float* out_perm;            // [P][d]
-  float* shared_out;          // [T][d]
+  void* out_perm;             // [P][d] bf16 or fp32
+  void* shared_out;           // [T][d]
+  bool out_bf16;
   int T, d, E, k, f, fs;
   unsigned* status;
 };
@@ -247,11 +248,11 @@ __global__ void __launch_bounds__(kSimtThreads) ffn2_simt_kernel(FfnArgs a) {
   for (int i = 0; i < 2; ++i) {
     const int r = ty + 16 * i;
     if (r >= ti.rows) continue;
-    float* orow = shared_grp ? a.shared_out + static_cast<size_t>(ti.row0 + r) * a.d
-                             : a.out_perm + static_cast<size_t>(ti.base + ti.row0 + r) * a.d;
+    void* outp = shared_grp ? a.shared_out : a.out_perm;
+    const size_t orow = static_cast<size_t>(shared_grp ? ti.row0 + r : ti.base + ti.row0 + r) * a.d;
     const float gw = s_gate[r];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) orow[n0 + tx + 16 * j] = acc[i][j] * gw;
+    for (int j = 0; j < 4; ++j) store_out(outp, orow + n0 + tx + 16 * j, acc[i][j] * gw, a.out_bf16);
   }
 }
 
@@ -261,8 +262,8 @@ size_t ffn_simt_ws_bytes(int T, int k, int f, int fs) {
 }
 
 cudaError_t launch_ffn_simt(const void* x, bool x_bf16, int w_dtype, const float* topk_w, const int32_t* offsets,
-                            const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
-                            int T, int d, int E, int k, int f, int fs, void* ws, unsigned* status,
+                            const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
+                            bool out_bf16, int T, int d, int E, int k, int f, int fs, void* ws, unsigned* status,
                             cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   FfnArgs a;
@@ -270,7 +271,7 @@ cudaError_t launch_ffn_simt(const void* x, bool x_bf16, int w_dtype, const float
   const size_t P = static_cast<size_t>(T) * k;
   a.h = static_cast<float*>(ws);
   a.hs = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(sizeof(float) * P * f, 256));
-  a.out_perm = out_perm; a.shared_out = shared_out;
+  a.out_perm = out_perm; a.shared_out = shared_out; a.out_bf16 = out_bf16;
   a.T = T; a.d = d; a.E = E; a.k = k; a.f = f; a.fs = fs; a.status = status;
   // upper bound of (group, 32-row) tiles: sum_e ceil(c_e/32) <= P/32 + E, plus the shared group
   const int tiles = static_cast<int>(P / kTM) + E + ceil_div(T, kTM) + 1;

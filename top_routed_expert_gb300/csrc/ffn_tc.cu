@@ -65,8 +65,9 @@ struct TcArgs {
   const float* as_scale;       // shared: s13_scale [2fs] | s2_scale [d]
   const float* b_scale;        // per-row activation scale [P+T]
   __nv_bfloat16* h;            // gemm1 out: H [(P+T)][fmax]
-  float* out_perm;             // gemm2 out: [P][d]
-  float* shared_out;           // gemm2 out: [T][d]
+  void* out_perm;              // gemm2 out: [P][d] bf16 or fp32
+  void* shared_out;            // gemm2 out: [T][d]
+  bool out_bf16;
   int T, k, E, P, d, f, fs, fmax;
   int TN;                      // token rows per tile; MMA N = 2*TN
   int stages, acc_bufs, tmem_cols;
@@ -114,10 +115,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     mbar_init(smem_u32(&c->ep_sync), kEpiThreads);
     c->abort = 0;
     fence_barrier_init();
-    // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
-    if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kBM, a.fs / kBM, a.status);
-    else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kBM, a.d / kBM, a.status);
   }
+  // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
+  if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kBM, a.fs / kBM, a.status);
+  else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kBM, a.d / kBM, a.status);
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
     tmem_relinquish();
@@ -294,8 +295,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       } else {
         const float sw = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * a.d + col];
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
-        float* outb = shr ? a.shared_out + (static_cast<size_t>(t.row0 - a.P) * a.d + col)
-                          : a.out_perm + (static_cast<size_t>(t.row0) * a.d + col);
+        void* outp = shr ? a.shared_out : a.out_perm;
+        const size_t out0 = static_cast<size_t>(shr ? t.row0 - a.P : t.row0) * a.d + col;
         // chunks of 64 columns = 32 token rows
         for (int c0 = 64 * half; c0 < N; c0 += 128) {
           float d0[32], d1[32], cf[32];
@@ -308,7 +309,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             if (j < t.nrows) {
               const float* dv = jj < 16 ? d0 : d1;
               const int q = 2 * (jj & 15);
-              outb[static_cast<size_t>(j) * a.d] = (dv[q] + dv[q + 1] * 0.0625f) * cf[jj] * sw;
+              store_out(outp, out0 + static_cast<size_t>(j) * a.d, (dv[q] + dv[q + 1] * 0.0625f) * cf[jj] * sw,
+                        a.out_bf16);
             }
           }
         }
@@ -487,8 +489,7 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUt
   a.tmem_cols = cols;
   size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + sizeof(TcCtrl);
   smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
-  cudaError_t err = cudaFuncSetAttribute(ffn_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_tc_kernel<MODE>), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const long long tiles_ub =
       static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
@@ -508,7 +509,7 @@ bool ffn_tc_supported(const moe_config_t& c) {
 size_t ffn_tc_ws_bytes(const moe_config_t& c) { return plan(c).total; }
 
 cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
-                          const int32_t* sorted_pair, const moe_weights_t* w, float* out_perm, float* shared_out,
+                          const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
                           void* ws, unsigned* status, int num_sms, cudaStream_t stream) {
   const int T = c.T, k = c.top_k, E = c.n_experts, d = c.d_model, f = c.d_ff, fs = c.d_ff_shared;
   if (T == 0) return cudaSuccess;
@@ -533,6 +534,7 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   TcArgs a = {};
   a.offsets = offsets; a.sorted_pair = sorted_pair; a.topk_w = topk_w;
   a.h = h; a.out_perm = out_perm; a.shared_out = shared_out;
+  a.out_bf16 = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0;
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
   a.TN = pl.TN; a.status = status;
 

@@ -13,10 +13,12 @@
 //
 // GB300 design: a CTA owns TOK tokens and all E experts for a slice of the
 // hidden dimension; the S CTAs of a thread-block cluster split the hidden
-// dimension and the cluster's rank-0 CTA sums their partial logits out of
-// distributed shared memory in rank order (deterministic), adds the bias and
-// runs a warp-per-token register top-k (k rounds of a warp arg-max keyed on
-// (logit desc, index asc)).  Inside a CTA one thread owns one expert (two when
+// dimension.  Each token has an owner rank; every rank stores its partial
+// logits of that token into the owner's shared memory (distributed shared
+// memory stores, no remote loads), and after one cluster barrier the owner
+// sums them in rank order (deterministic), adds the bias and runs a warp
+// register top-k (k rounds of a warp arg-max keyed on (logit desc, index
+// asc)).  Inside a CTA one thread owns one expert (two when
 // E > 128) and keeps all TOK token sums in registers; chunks of W_r and x are
 // staged with cp.async, double-buffered, and read back as float4 (W_r rows
 // padded by 4 floats so a warp's 32 row reads spread over all banks; x reads
@@ -64,7 +66,10 @@ struct RouterSmem {
   static constexpr size_t kWStage = static_cast<size_t>(EMAX) * kRouterWPitch * sizeof(float);   // bytes
   static constexpr size_t kXStage = (static_cast<size_t>(TOK) * XStage<XT>::kPitch * sizeof(XT) + 15) / 16 * 16;
   static constexpr size_t kStage = kWStage + kXStage;
-  static constexpr size_t kPost = 2 * static_cast<size_t>(TOK) * EMAX * sizeof(float);
+  // after the staging buffers: the receive buffer [S][ceil(TOK/S)][EMAX]
+  // (S * ceil(TOK/S) <= TOK + 16 rows) and one summed row per warp
+  static constexpr size_t kRecv = static_cast<size_t>(TOK + 16) * EMAX * sizeof(float);
+  static constexpr size_t kRows = 4 * static_cast<size_t>(EMAX) * sizeof(float);
 };
 
 // TOK tokens per CTA, EPT experts per thread (E <= 128*EPT), NBUF staging buffers.
@@ -77,10 +82,10 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   constexpr int EMAX = L::EMAX;
   constexpr int XP = XStage<XT>::kPitch;
   extern __shared__ __align__(16) uint8_t smem_u8[];
-  // stage b: [W_r chunk EMAX x (KC+4) floats][x chunk TOK x XP]; after the
-  // main loop the area is reused for the partial and summed logits.
-  float* lp = reinterpret_cast<float*>(smem_u8);      // [TOK][EMAX] partial logits (read by rank 0)
-  float* ls = lp + TOK * EMAX;                         // [TOK][EMAX] rank 0: summed logits
+  // [NBUF stages: W_r chunk EMAX x (KC+4) floats | x chunk TOK x XP]
+  // [recv: partial logits pushed here by every rank] [one summed row per warp]
+  float* recv = reinterpret_cast<float*>(smem_u8 + NBUF * L::kStage);
+  float* rows = recv + (TOK + 16) * EMAX;
 
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned S = cluster.num_blocks();
@@ -91,6 +96,10 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   const int kbeg = min(d, static_cast<int>(rank) * kslice);
   const int kend = min(d, kbeg + kslice);
   const int nchunks = (kend - kbeg) / kRouterKC;
+
+  // distributed shared memory may only be touched once every CTA of the
+  // cluster runs: arrive now, wait before the first remote store
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   auto wstage = [&](int buf) { return reinterpret_cast<float*>(smem_u8 + buf * L::kStage); };
   auto xstage = [&](int buf) { return reinterpret_cast<XT*>(smem_u8 + buf * L::kStage + L::kWStage); };
@@ -161,34 +170,38 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   cp_async_wait<0>();
   __syncthreads();
 
+  // Push: token b is owned by rank b % S (local slot b / S); every rank
+  // stores its partial logits of b into the owner's receive buffer at
+  // [my rank][slot][expert] through distributed shared memory.  The receive
+  // buffer is never used for staging, so no rank can overwrite live data.
+  const int slots = (TOK + static_cast<int>(S) - 1) / static_cast<int>(S);
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 #pragma unroll
-  for (int a = 0; a < EPT; ++a)
+  for (int b = 0; b < TOK; ++b) {
+    const unsigned owner = static_cast<unsigned>(b) % S;
+    float* dst = cluster.map_shared_rank(recv, owner) + (rank * slots + b / static_cast<int>(S)) * EMAX;
 #pragma unroll
-    for (int b = 0; b < TOK; ++b) lp[b * EMAX + tid + kRouterThreads * a] = acc[a][b];
-
-  cluster.sync();   // all partial logits of the cluster are in shared memory
-  if (rank == 0) {
-    for (int i = tid; i < TOK * EMAX; i += kRouterThreads) {
-      const int e = i % EMAX;
-      float s = 0.f;
-      for (unsigned q = 0; q < S; ++q) {
-        const float* remote = cluster.map_shared_rank(lp, q);
-        s += remote[i];
-      }
-      if (e < E && bias) s += bias[e];
-      ls[i] = s;
-    }
+    for (int a = 0; a < EPT; ++a) dst[tid + kRouterThreads * a] = acc[a][b];
   }
-  cluster.sync();   // peers may exit only after rank 0 has read their partials
-  if (rank != 0) return;
-
-  // Top-k: one warp per token.
+  cluster.sync();   // every partial row has arrived at its owner
+  // One warp per owned token: sum the S partial rows in rank order
+  // (deterministic), add the bias, select.
   const int warp = tid >> 5, lane = tid & 31;
-  for (int r = warp; r < TOK; r += kRouterThreads / 32) {
-    const int t = t0 + r;
-    if (t >= T) break;
-    warp_topk_token<EMAX / 32>(ls + r * EMAX, E, k, lane, ids + static_cast<size_t>(t) * k,
-                               gates + static_cast<size_t>(t) * k, status);
+  float* lrow = rows + warp * EMAX;
+  for (int sl = warp; sl < slots; sl += 4) {
+    const int b = sl * static_cast<int>(S) + static_cast<int>(rank);
+    const int t = t0 + b;
+    if (b >= TOK || t >= T) break;
+    for (int e = lane; e < EMAX; e += 32) {
+      float v = 0.f;
+      for (unsigned q = 0; q < S; ++q) v += recv[(q * slots + sl) * EMAX + e];
+      if (e < E && bias) v += bias[e];
+      lrow[e] = v;
+    }
+    __syncwarp();
+    warp_topk_token<EMAX / 32>(lrow, E, k, lane, ids + static_cast<size_t>(t) * k, gates + static_cast<size_t>(t) * k,
+                               status);
+    __syncwarp();
   }
 }
 
@@ -199,10 +212,10 @@ static cudaError_t launch_router_t(const void* x, const float* wr, const float* 
   const int tiles = ceil_div(T, TOK);
   // hidden-dim slice per cluster rank, a multiple of the staging chunk
   const int kslice = ceil_div(ceil_div(d, S), kRouterKC) * kRouterKC;
-  constexpr size_t smem = (NBUF * L::kStage > L::kPost) ? NBUF * L::kStage : L::kPost;
+  constexpr size_t smem = NBUF * L::kStage + L::kRecv + L::kRows;
   static_assert(smem <= 227 * 1024, "router staging exceeds shared memory");
-  cudaError_t err = cudaFuncSetAttribute(router_kernel<XT, TOK, EPT, NBUF>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(router_kernel<XT, TOK, EPT, NBUF>),
+                                        static_cast<int>(smem), S > 8);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * S);
@@ -222,8 +235,8 @@ static cudaError_t launch_router_t(const void* x, const float* wr, const float* 
 }
 
 // Chooses tokens-per-CTA and the cluster split so that small T still spreads
-// over the SMs: S ranks split d (up to 8, the portable cluster size), each rank
-// at least one staging chunk.
+// over the SMs: S ranks split d (up to 16, a non-portable cluster size the
+// GPU supports), each rank at least one staging chunk.
 cudaError_t launch_router(const void* x, bool x_bf16, const float* wr, const float* bias, int T, int d, int E,
                           int k, int32_t* ids, float* w, unsigned* status, int num_sms, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
@@ -231,7 +244,7 @@ cudaError_t launch_router(const void* x, bool x_bf16, const float* wr, const flo
   const int TOK = big ? 32 : 8;
   const int tiles = ceil_div(T, TOK);
   int S = 1;
-  while (S < 8 && tiles * S < num_sms && d / (2 * S) >= kRouterKC) S *= 2;
+  while (S < 16 && tiles * S < num_sms && d / (2 * S) >= kRouterKC) S *= 2;
   const bool e128 = E <= 128;
 #define MOE_ROUTER_CASE(XT, TOKC, EPT, NB) \
   return launch_router_t<XT, TOKC, EPT, NB>(x, wr, bias, T, d, E, k, S, ids, w, status, stream)

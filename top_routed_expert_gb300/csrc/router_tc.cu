@@ -268,7 +268,7 @@ cudaError_t launch_router_tc(const void* x, const float* wr, const float* bias, 
   const size_t smem = 1024 + kRtStages * static_cast<size_t>(kRtStage) + sizeof(RtCtrl);
   static_assert(kRtStages * kRtStage >= static_cast<uint32_t>(kRtTok * kRtLPitch * 4),
                 "the logits tile reuses the pipeline stages");
-  err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  err = ensure_kernel_attrs(reinterpret_cast<const void*>(router_tc_kernel), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   count_launches(1);
   router_tc_kernel<<<ceil_div(T, kRtTok), kRtThreads, smem, stream>>>(mW, mX, bias, T, d, E, k, ids, w, status);

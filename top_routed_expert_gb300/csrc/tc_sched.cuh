@@ -37,11 +37,14 @@ __device__ __forceinline__ Tile decode_tile(const GroupTable& gt, int G, int i, 
 // Fills the table for E routed groups plus the shared group; wtiles_routed /
 // wtiles_shared weight tiles per group, token tiles of TN rows.  Offsets that
 // are not monotone or leave [0, P] make that group empty and record
-// MOE_ERR_DEVICE_BOUNDS.  Returns the number of tiles.  One thread.
-__device__ __forceinline__ int build_group_table(GroupTable& gt, const int32_t* offsets, int E, int P, int T, int TN,
-                                                 int wtiles_routed, int wtiles_shared, unsigned* status) {
-  int acc = 0;
-  for (int g = 0; g <= E; ++g) {
+// MOE_ERR_DEVICE_BOUNDS.  Called by every thread of the block (it contains
+// __syncthreads): one thread per group fills the group's entries, then warp 0
+// turns the per-group tile counts into their exclusive prefix sum with warp
+// shuffles.  Returns after the table is visible to the whole block.
+__device__ __forceinline__ void build_group_table(GroupTable& gt, const int32_t* offsets, int E, int P, int T, int TN,
+                                                  int wtiles_routed, int wtiles_shared, unsigned* status) {
+  const int G = E + 1;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
     int base, rows;
     if (g < E) {
       base = offsets[g];
@@ -55,16 +58,31 @@ __device__ __forceinline__ int build_group_table(GroupTable& gt, const int32_t* 
       base = P;
       rows = T;
     }
-    const int wt = (g < E) ? wtiles_routed : wtiles_shared;
     const int mt = (rows + TN - 1) / TN;
-    gt.tile_start[g] = acc;
     gt.row_base[g] = base;
     gt.rows[g] = rows;
     gt.mtiles[g] = mt;
-    acc += mt * wt;
+    gt.tile_start[g] = mt * ((g < E) ? wtiles_routed : wtiles_shared);   // tile count, scanned below
   }
-  gt.tile_start[E + 1] = acc;
-  return acc;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int c0 = 0; c0 < G; c0 += 32) {
+      const int g = c0 + lane;
+      const int cnt = (g < G) ? gt.tile_start[g] : 0;
+      int v = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+      }
+      if (g < G) gt.tile_start[g] = carry + v - cnt;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) gt.tile_start[G] = carry;
+  }
+  __syncthreads();
 }
 
 }  // namespace moe
