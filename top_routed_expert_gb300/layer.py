@@ -83,6 +83,29 @@ class MoELayer:
             return y, ids, w, offs
         return y
 
+    def capture(self, x: torch.Tensor, y: Optional[torch.Tensor] = None, warmup: int = 2):
+        """Record one layer pass over the device buffers x -> y as a CUDA graph.
+
+        Returns (graph, y); graph.replay() re-runs the whole layer (all its
+        kernels) on whatever x holds at replay time.  Kernel attributes and the
+        workspace are set up by the warm-up passes, so nothing is created while
+        capturing.
+        """
+        T = x.shape[0]
+        if y is None:
+            y = self.empty_y(T)
+        self.workspace(T)
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                self.forward(x, y, stream=side)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            self.forward(x, y, stream=side)
+        return graph, y
+
     def forward_host(self, x_host: torch.Tensor, y_host: torch.Tensor, x_dev: torch.Tensor,
                      y_dev: torch.Tensor, stream=None):
         """End to end from host buffers: H2D copy of x, the layer, D2H copy of y.
