@@ -63,6 +63,12 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtyp
 #define MOE_FLAG_SIMT_FFN 0x1u     /* run the expert FFN on the CUDA-core kernels */
 #define MOE_FLAG_SIMT_ROUTER 0x2u  /* run the router on the CUDA-core kernel       */
 #define MOE_FLAG_BF16_EXPERT_OUT 0x4u  /* out_perm / shared_out in bf16 (default fp32) */
+/* Test hook for the failure path: in the tensor-core expert GEMM, CTA 0
+ * withholds one "accumulator ready" signal and every bounded wait shortens to
+ * 20 ms, so the epilogue's wait runs out; the kernel drains its copies and
+ * MMAs, frees tensor memory and returns, and moe_get_device_status() reports
+ * MOE_ERR_DEVICE_TIMEOUT.  The outputs of that call are not valid. */
+#define MOE_FLAG_INJECT_TIMEOUT 0x100u
 
 typedef struct {
   int32_t T;            /* tokens, >= 0 (0 is a no-op)                          */

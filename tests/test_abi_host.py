@@ -136,3 +136,9 @@ def test_no_cuda_device_reports_error(lib):
     c = cfg()
     fake = ctypes.c_void_p(0x10000)
     assert lib.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, None, 0, None) in (4, 7)
+
+
+def test_test_hook_flag_is_accepted(lib):
+    assert lib.moe_workspace_bytes(ctypes.byref(cfg(flags=abi.MOE_FLAG_INJECT_TIMEOUT))) > 0
+    assert lib.moe_workspace_bytes(ctypes.byref(cfg(flags=abi.MOE_FLAG_BF16_EXPERT_OUT))) < \
+        lib.moe_workspace_bytes(ctypes.byref(cfg()))

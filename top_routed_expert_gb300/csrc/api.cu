@@ -102,7 +102,7 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_E4M3 && c->w_dtype != MOE_NVFP4) return MOE_ERR_INVALID_ARG;
   if (c->y_dtype != MOE_F32 && c->y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(c->T) * c->top_k > (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER | MOE_FLAG_BF16_EXPERT_OUT)) != 0)
+  if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER | MOE_FLAG_BF16_EXPERT_OUT | MOE_FLAG_INJECT_TIMEOUT)) != 0)
     return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }

@@ -468,7 +468,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
 // One warp per row of the (P+T)-row space; GATHER_X takes row r < P from
 // x[sorted_pair[r]/k] and row P+t from x[t], else row r of H (width f for
 // routed rows, f_s for shared rows).
-template <bool GATHER_X>
+template <bool GATHER_X, bool IN_REGS>
 __global__ void __launch_bounds__(256)
 scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                     int width_r, int width_s, int src_stride, __half* __restrict__ dst, int dst_stride,
@@ -497,15 +497,30 @@ scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict_
     s = src + static_cast<size_t>(row) * src_stride;
     width = row < P ? width_r : width_s;
   }
+  // Rows up to kRegChunks * 256 elements are read once into registers; longer
+  // rows take a second pass from L2.
+  constexpr int kRegChunks = 16;
+  uint4 reg[IN_REGS ? kRegChunks : 1];
+  const bool in_regs = IN_REGS && width <= kRegChunks * 256;
   float amax = 0.f;
-  for (int c = lane * 8; c < width; c += 256) {
-    const uint4 v = *reinterpret_cast<const uint4*>(s + c);
+  auto absmax8 = [&](const uint4& v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    for (int q = 0; q < 4; ++q) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xffff0000u)));
     }
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < (IN_REGS ? kRegChunks : 1); ++i) {
+      const int c = lane * 8 + i * 256;
+      reg[i] = (c < width) ? *reinterpret_cast<const uint4*>(s + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < (IN_REGS ? kRegChunks : 1); ++i) absmax8(reg[i]);
+  } else {
+    for (int c = lane * 8; c < width; c += 256) absmax8(*reinterpret_cast<const uint4*>(s + c));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -516,8 +531,7 @@ scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict_
     sc = ldexpf(1.0f, e - 14);
   }
   const float inv = 1.0f / sc;   // exact: a power of two
-  for (int c = lane * 8; c < width; c += 256) {
-    const uint4 v = *reinterpret_cast<const uint4*>(s + c);
+  auto emit = [&](int c, const uint4& v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
@@ -526,6 +540,15 @@ scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict_
       o[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
     *reinterpret_cast<uint4*>(drow + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < (IN_REGS ? kRegChunks : 1); ++i) {
+      const int c = lane * 8 + i * 256;
+      if (c < width) emit(c, reg[i]);
+    }
+  } else {
+    for (int c = lane * 8; c < width; c += 256) emit(c, *reinterpret_cast<const uint4*>(s + c));
   }
   if (lane == 0) scale[row] = sc;
 }
@@ -635,9 +658,14 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   float* sh = reinterpret_cast<float*>(base + pl.sh);
 
   const int qblocks = ceil_div(R, 8);
+  const bool regs = R <= 4096;   // see the FP8 path: registers for few rows, two passes for many
   count_launches(1);
-  scale16_rows_kernel<true><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d,
-                                                         d, d, xh, d, sx, status);
+  if (regs)
+    scale16_rows_kernel<true, true><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T,
+                                                                 k, d, d, d, xh, d, sx, status);
+  else
+    scale16_rows_kernel<true, false><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T,
+                                                                  k, d, d, d, xh, d, sx, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
@@ -658,8 +686,12 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   if (err != cudaSuccess) return err;
 
   count_launches(1);
-  scale16_rows_kernel<false><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P, T, k, f,
-                                                          fs, fmax, hh, fmax, sh, status);
+  if (regs)
+    scale16_rows_kernel<false, true><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P, T,
+                                                                  k, f, fs, fmax, hh, fmax, sh, status);
+  else
+    scale16_rows_kernel<false, false><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P,
+                                                                   T, k, f, fs, fmax, hh, fmax, sh, status);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 

@@ -71,6 +71,8 @@ struct TcArgs {
   int T, k, E, P, d, f, fs, fmax;
   int TN;                      // token rows per tile; MMA N = 2*TN
   int stages, acc_bufs, tmem_cols;
+  uint64_t wait_ns;            // limit of every bounded wait
+  int inject_drop;             // test hook: CTA 0 withholds its first "accumulator ready"
   unsigned* status;
 };
 
@@ -156,7 +158,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         }
         const int brow = 2 * t.row0;
         for (int kb = 0; kb < K / kBK; ++kb) {
-          if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, kWaitLimitNs)) break;
+          if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, a.wait_ns)) break;
           const uint32_t full = smem_u32(&c->full[st]);
           mbar_arrive_expect_tx(full, NA * kABytes + b_bytes);
           const uint32_t sA = smem_u32(smem + st * stage_bytes);
@@ -187,12 +189,12 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const Tile t = decode_tile(c->gt, G, i, a.TN);
         const bool shr = t.g == a.E;
         const int K = (MODE == 1) ? a.d : (shr ? a.fs : a.f);
-        if (!mbar_wait(smem_u32(&c->tempty[ab]), aph ^ 1u, abort, kWaitLimitNs)) break;
+        if (!mbar_wait(smem_u32(&c->tempty[ab]), aph ^ 1u, abort, a.wait_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + static_cast<uint32_t>(ab * NA * N);
         const uint32_t d1 = d0 + static_cast<uint32_t>(N);
         for (int kb = 0; kb < K / kBK; ++kb) {
-          if (!mbar_wait(smem_u32(&c->full[st]), ph, abort, kWaitLimitNs)) {
+          if (!mbar_wait(smem_u32(&c->full[st]), ph, abort, a.wait_ns)) {
             ok = false;
             break;
           }
@@ -214,7 +216,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&c->tfull[ab]));
+        if (!(a.inject_drop && blockIdx.x == 0 && i == static_cast<int>(blockIdx.x)))
+          mma_commit(smem_u32(&c->tfull[ab]));
         if (++ab == a.acc_bufs) {
           ab = 0;
           aph ^= 1u;
@@ -262,11 +265,11 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       // all coefficients written (bounded wait: a warp that gave up cannot
       // leave the others blocked)
       mbar_arrive(smem_u32(&c->ep_sync));
-      if (!mbar_wait(smem_u32(&c->ep_sync), eph, abort, kWaitLimitNs)) break;
+      if (!mbar_wait(smem_u32(&c->ep_sync), eph, abort, a.wait_ns)) break;
       eph ^= 1u;
       const float* coef = c->coef[cb_par];
       cb_par ^= 1;
-      if (!mbar_wait(smem_u32(&c->tfull[ab]), aph, abort, kWaitLimitNs)) break;
+      if (!mbar_wait(smem_u32(&c->tfull[ab]), aph, abort, a.wait_ns)) break;
       tc_fence_after();
       const int col = t.wt * kBM + n;
       if (MODE == 1) {
@@ -337,7 +340,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
 // (P+T)-row activation space.  GATHER_X: row r < P takes x[sorted_pair[r]/k],
 // row P+t takes x[t] (width d); otherwise row r of H (width f for routed
 // rows, f_s for shared rows).  Output q[2r] = hi codes, q[2r+1] = lo codes.
-template <bool GATHER_X>
+template <bool GATHER_X, bool IN_REGS>
 __global__ void __launch_bounds__(256)
 quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                    int width_r, int width_s, int src_stride, uint8_t* __restrict__ q, int q_stride,
@@ -370,14 +373,36 @@ quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__
     s = src + static_cast<size_t>(row) * src_stride;
     width = row < P ? width_r : width_s;
   }
+  // Rows up to kRegChunks * 256 elements are read once into registers (all
+  // loads in flight together); longer rows take a second pass from L2.
+  constexpr int kRegChunks = 16;
+  uint4 reg[IN_REGS ? kRegChunks : 1];
+  const bool in_regs = IN_REGS && width <= kRegChunks * 256;
   float amax = 0.f;
-  for (int c = lane * 8; c < width; c += 256) {
-    const uint4 v = *reinterpret_cast<const uint4*>(s + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if (in_regs) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    for (int i = 0; i < (IN_REGS ? kRegChunks : 1); ++i) {
+      const int c = lane * 8 + i * 256;
+      reg[i] = (c < width) ? *reinterpret_cast<const uint4*>(s + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < (IN_REGS ? kRegChunks : 1); ++i) {
+      const uint32_t w[4] = {reg[i].x, reg[i].y, reg[i].z, reg[i].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xffff0000u)));
+      }
+    }
+  } else {
+    for (int c = lane * 8; c < width; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(s + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xffff0000u)));
+      }
     }
   }
 #pragma unroll
@@ -390,8 +415,7 @@ quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__
     if (amax / sc > 448.0f) sc *= 2.0f;
   }
   const float inv = 1.0f / sc;   // exact: sc is a power of two
-  for (int c = lane * 8; c < width; c += 256) {
-    const uint4 v = *reinterpret_cast<const uint4*>(s + c);
+  auto emit = [&](int c, const uint4& v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t hi[2] = {0, 0}, lo[2] = {0, 0};
 #pragma unroll
@@ -407,6 +431,15 @@ quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__
     }
     *reinterpret_cast<uint2*>(qh + c) = make_uint2(hi[0], hi[1]);
     *reinterpret_cast<uint2*>(ql + c) = make_uint2(lo[0], lo[1]);
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < (IN_REGS ? kRegChunks : 1); ++i) {
+      const int c = lane * 8 + i * 256;
+      if (c < width) emit(c, reg[i]);
+    }
+  } else {
+    for (int c = lane * 8; c < width; c += 256) emit(c, *reinterpret_cast<const uint4*>(s + c));
   }
   if (lane == 0) scale[row] = sc;
 }
@@ -523,10 +556,17 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   uint8_t* hq = reinterpret_cast<uint8_t*>(base + pl.hq);
   float* sh = reinterpret_cast<float*>(base + pl.sh);
 
+  // few rows (decode): keep each row in registers (one read, all loads in
+  // flight); many rows: a lean two-pass kernel keeps more warps resident
   const int qblocks = ceil_div(R, 8);
+  const bool regs = R <= 4096;
   count_launches(1);
-  quant2_rows_kernel<true><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d, d,
-                                                        d, xq, d, sx, status);
+  if (regs)
+    quant2_rows_kernel<true, true><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T, k,
+                                                                d, d, d, xq, d, sx, status);
+  else
+    quant2_rows_kernel<true, false><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T,
+                                                                 k, d, d, d, xq, d, sx, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
@@ -537,6 +577,9 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   a.out_bf16 = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0;
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
   a.TN = pl.TN; a.status = status;
+  const bool inject = (c.flags & MOE_FLAG_INJECT_TIMEOUT) != 0;
+  a.wait_ns = inject ? 20000000ull : kWaitLimitNs;
+  a.inject_drop = inject ? 1 : 0;
 
   // gemm1: gate/up
   if (!make_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, kBM) ||
@@ -551,8 +594,12 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   if (err != cudaSuccess) return err;
 
   count_launches(1);
-  quant2_rows_kernel<false><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P, T, k, f,
-                                                         fs, fmax, hq, fmax, sh, status);
+  if (regs)
+    quant2_rows_kernel<false, true><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P, T,
+                                                                 k, f, fs, fmax, hq, fmax, sh, status);
+  else
+    quant2_rows_kernel<false, false><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P,
+                                                                  T, k, f, fs, fmax, hq, fmax, sh, status);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
