@@ -54,7 +54,7 @@ typedef enum {
   MOE_ERR_DEVICE_TIMEOUT = 5,   /* a bounded device-side wait ran out          */
   MOE_ERR_DEVICE_BOUNDS = 6,    /* an index read on the device was out of range */
   MOE_ERR_ARCH = 7,             /* current device is not sm_103                */
-  MOE_ERR_DEVICE_NONFINITE = 8  /* a router row had no finite logit            */
+  MOE_ERR_DEVICE_NONFINITE = 8  /* a router row held a non-finite logit        */
 } moe_status_t;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtype_t;
@@ -142,6 +142,9 @@ size_t moe_workspace_bytes(const moe_config_t* cfg);
  *               logits on the tensor cores (W_r split exactly into three bf16
  *               terms held in the workspace); otherwise (or with ws NULL) the
  *               CUDA-core router runs.  Both give fp32-accurate logits.
+ * A token whose logits include a non-finite value (from a non-finite input)
+ * is routed among its finite logits only and raises
+ * MOE_ERR_DEVICE_NONFINITE in the device status word.
  */
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const float* w_router,
                        const float* expert_bias, int32_t* topk_ids, float* topk_w,

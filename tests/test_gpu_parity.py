@@ -190,6 +190,56 @@ def test_router_alone_with_bias():
     _, o = check_routing(inp, ids_np, w_np, oracle.permute(ids_np, 64)[1])
 
 
+def _route(inp, x=None):
+    layer = MoELayer(inp)
+    T, k = inp.cfg.T, inp.cfg.k
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    abi.moe_route(layer.config(), device_x(inp) if x is None else x, layer.w_router, layer.bias, ids, w,
+                  layer.workspace())
+    return ids.cpu().numpy(), w.cpu().numpy(), abi.moe_get_device_status()
+
+
+# T = 77 runs the CUDA-core router, T = 1100 the tensor-core router
+@pytest.mark.parametrize("T", [77, 1100])
+def test_exact_ties_take_the_lower_expert(T):
+    # identical router rows give bitwise-equal logits in both routers (same
+    # operands, same accumulation order): the lower expert index must come
+    # first whenever the higher one is picked
+    E, k = 16, 4
+    inp = moe_synth.make_custom(T=T, d=256, E=E, k=k, f=64, fs=64, x_dtype="bf16", w_dtype="e4m3", seed=T)
+    twins = {5: 2, 9: 2, 12: 7}
+    for hi, lo in twins.items():
+        inp.w_router[hi] = inp.w_router[lo]
+    ids, w, st = _route(inp)
+    assert st == 0
+    hits = 0
+    for t in range(T):
+        row = list(ids[t])
+        for hi, lo in twins.items():
+            if hi in row:
+                assert lo in row and row.index(lo) < row.index(hi), (t, row)
+                assert w[t, row.index(lo)] == w[t, row.index(hi)]
+                hits += 1
+    assert hits > 0
+
+
+@pytest.mark.parametrize("T", [77, 1100])
+def test_nonfinite_input_is_reported(T):
+    # a token with an infinite input has no finite logit: the status word
+    # says so, and every other token routes exactly as in a clean run
+    inp = moe_synth.make_custom(T=T, d=256, E=32, k=4, f=64, fs=64, x_dtype="bf16", w_dtype="e4m3", seed=3)
+    ids0, w0, st0 = _route(inp)
+    assert st0 == 0
+    x = device_x(inp)
+    x[3, 0] = 0x7F80    # bf16 +inf bit pattern
+    ids1, w1, st1 = _route(inp, x)
+    assert st1 == 8     # MOE_ERR_DEVICE_NONFINITE
+    keep = np.arange(T) != 3
+    assert np.array_equal(ids0[keep], ids1[keep]) and np.array_equal(w0[keep], w1[keep])
+    assert abi.moe_get_device_status() == 0     # cleared
+
+
 # Shapes whose average rows per expert select each tensor-core token tile
 # (TN = 8, 16, 32, 64, 128) with ragged last tiles, f != f_s, and a d that is
 # not a power of two.

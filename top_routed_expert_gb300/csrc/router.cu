@@ -16,13 +16,19 @@
 // dimension.  Each token has an owner rank; every rank stores its partial
 // logits of that token into the owner's shared memory (distributed shared
 // memory stores, no remote loads), and after one cluster barrier the owner
-// sums them in rank order (deterministic), adds the bias and runs a warp
-// register top-k (k rounds of a warp arg-max keyed on (logit desc, index
-// asc)).  Inside a CTA one thread owns one expert (two when
-// E > 128) and keeps all TOK token sums in registers; chunks of W_r and x are
-// staged with cp.async, double-buffered, and read back as float4 (W_r rows
-// padded by 4 floats so a warp's 32 row reads spread over all banks; x reads
-// are broadcasts).  Logits stay fp32 from bf16/fp32 inputs.
+// sums them in rank order (deterministic), adds the bias and runs the warp
+// top-k (redux-based arg-max rounds, one warp per token).
+//
+// Inside a CTA of 256 threads a thread owns one expert and keeps all TOK
+// token sums in registers.  With E <= 128 the threads form two groups that
+// take alternate 8-column steps of every staged chunk (two warps per SM
+// sub-partition share the FMA work), and group 1 hands its sums to group 0
+// through shared memory at the end.  Chunks of 64 hidden columns of W_r and
+// x are staged with cp.async, double-buffered (about 36 KB a stage, so two
+// CTAs fit on an SM and a 16-CTA cluster always finds room), and read back as
+// float4 (W_r rows padded by 4 floats so a warp's 32 row reads spread over
+// all banks; x reads are broadcasts).  Logits stay fp32 from bf16/fp32
+// inputs.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -32,8 +38,8 @@ namespace cg = cooperative_groups;
 
 namespace moe {
 
-constexpr int kRouterThreads = 128;
-constexpr int kRouterKC = 128;            // hidden-dim chunk per pipeline stage
+constexpr int kRouterThreads = 256;
+constexpr int kRouterKC = 64;             // hidden-dim chunk per pipeline stage
 constexpr int kRouterWPitch = kRouterKC + 4;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -50,41 +56,49 @@ struct XStage {          // x chunk row pitch in elements (16-byte aligned rows)
   static constexpr int kPitch = kRouterKC + 16 / static_cast<int>(sizeof(XT));
 };
 
-__device__ __forceinline__ void x4_to_float(const float* p, float (&v)[4]) {
-  const float4 q = *reinterpret_cast<const float4*>(p);
-  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+// eight consecutive x values as floats
+__device__ __forceinline__ void x8_to_float(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
-__device__ __forceinline__ void x4_to_float(const uint16_t* p, float (&v)[4]) {
-  const uint2 q = *reinterpret_cast<const uint2*>(p);
-  v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
-  v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
+__device__ __forceinline__ void x8_to_float(const uint16_t* p, float (&v)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
 }
 
-template <typename XT, int TOK, int EPT>
+template <typename XT, int TOK, int EMAX>
 struct RouterSmem {
-  static constexpr int EMAX = kRouterThreads * EPT;
+  static constexpr int KG = kRouterThreads / EMAX;   // column groups (2 for E <= 128, else 1)
   static constexpr size_t kWStage = static_cast<size_t>(EMAX) * kRouterWPitch * sizeof(float);   // bytes
   static constexpr size_t kXStage = (static_cast<size_t>(TOK) * XStage<XT>::kPitch * sizeof(XT) + 15) / 16 * 16;
   static constexpr size_t kStage = kWStage + kXStage;
-  // after the staging buffers: the receive buffer [S][ceil(TOK/S)][EMAX]
+  // after the two staging buffers: the receive buffer [S][ceil(TOK/S)][EMAX]
   // (S * ceil(TOK/S) <= TOK + 16 rows) and one summed row per warp
   static constexpr size_t kRecv = static_cast<size_t>(TOK + 16) * EMAX * sizeof(float);
-  static constexpr size_t kRows = 4 * static_cast<size_t>(EMAX) * sizeof(float);
+  static constexpr size_t kRows = (kRouterThreads / 32) * static_cast<size_t>(EMAX) * sizeof(float);
+  static constexpr size_t kTotal = 2 * kStage + kRecv + kRows;
+  static_assert(static_cast<size_t>(TOK) * EMAX * sizeof(float) <= 2 * kStage, "group hand-off exceeds staging");
 };
 
-// TOK tokens per CTA, EPT experts per thread (E <= 128*EPT), NBUF staging buffers.
-template <typename XT, int TOK, int EPT, int NBUF>
+// TOK tokens per CTA, EMAX = 128 or 256 experts per CTA (E <= EMAX).
+template <typename XT, int TOK, int EMAX>
 __global__ void __launch_bounds__(kRouterThreads)
 router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
               int T, int d, int E, int k, int kslice, int32_t* __restrict__ ids, float* __restrict__ gates,
               unsigned* status) {
-  using L = RouterSmem<XT, TOK, EPT>;
-  constexpr int EMAX = L::EMAX;
+  using L = RouterSmem<XT, TOK, EMAX>;
+  constexpr int KG = L::KG;
   constexpr int XP = XStage<XT>::kPitch;
   extern __shared__ __align__(16) uint8_t smem_u8[];
-  // [NBUF stages: W_r chunk EMAX x (KC+4) floats | x chunk TOK x XP]
+  // [2 stages: W_r chunk EMAX x (KC+4) floats | x chunk TOK x XP]
   // [recv: partial logits pushed here by every rank] [one summed row per warp]
-  float* recv = reinterpret_cast<float*>(smem_u8 + NBUF * L::kStage);
+  float* recv = reinterpret_cast<float*>(smem_u8 + 2 * L::kStage);
   float* rows = recv + (TOK + 16) * EMAX;
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -93,6 +107,8 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   const int tile = blockIdx.x / S;
   const int t0 = tile * TOK;
   const int tid = threadIdx.x;
+  const int e_own = tid % EMAX;     // this thread's expert
+  const int grp = tid / EMAX;       // its column group
   const int kbeg = min(d, static_cast<int>(rank) * kslice);
   const int kend = min(d, kbeg + kslice);
   const int nchunks = (kend - kbeg) / kRouterKC;
@@ -123,52 +139,52 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
     }
   };
 
-  float acc[EPT][TOK];
+  float acc[TOK];
 #pragma unroll
-  for (int a = 0; a < EPT; ++a)
-#pragma unroll
-    for (int b = 0; b < TOK; ++b) acc[a][b] = 0.f;
+  for (int b = 0; b < TOK; ++b) acc[b] = 0.f;
 
   if (nchunks > 0) stage_chunk(0, 0);
   cp_async_commit();
   for (int c = 0; c < nchunks; ++c) {
-    const int buf = (NBUF == 2) ? (c & 1) : 0;
-    if (NBUF == 2) {
-      if (c + 1 < nchunks) stage_chunk(c + 1, buf ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int buf = c & 1;
+    if (c + 1 < nchunks) stage_chunk(c + 1, buf ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
     __syncthreads();
-    const float* wb = wstage(buf);
+    const float* wrow = wstage(buf) + e_own * kRouterWPitch;
     const XT* xb = xstage(buf);
 #pragma unroll 2
-    for (int kk = 0; kk < kRouterKC; kk += 4) {
-      float w[EPT][4];
-#pragma unroll
-      for (int a = 0; a < EPT; ++a) {
-        const float4 q = *reinterpret_cast<const float4*>(wb + (tid + kRouterThreads * a) * kRouterWPitch + kk);
-        w[a][0] = q.x; w[a][1] = q.y; w[a][2] = q.z; w[a][3] = q.w;
-      }
+    for (int kk = grp * 8; kk < kRouterKC; kk += 8 * KG) {
+      const float4 wa = *reinterpret_cast<const float4*>(wrow + kk);
+      const float4 wb = *reinterpret_cast<const float4*>(wrow + kk + 4);
+      const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
       for (int b = 0; b < TOK; ++b) {
-        float xv[4];
-        x4_to_float(xb + b * XP + kk, xv);
+        float xv[8];
+        x8_to_float(xb + b * XP + kk, xv);
 #pragma unroll
-        for (int a = 0; a < EPT; ++a)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[a][b] = fmaf(xv[q], w[a][q], acc[a][b]);
+        for (int q = 0; q < 8; ++q) acc[b] = fmaf(xv[q], w[q], acc[b]);
       }
     }
     __syncthreads();
-    if (NBUF == 1 && c + 1 < nchunks) {
-      stage_chunk(c + 1, 0);
-      cp_async_commit();
-    }
   }
   cp_async_wait<0>();
   __syncthreads();
+
+  // column group 1 hands its sums to group 0 through the (now idle) staging
+  // buffers; group 0 adds them in a fixed order
+  if (KG == 2) {
+    float* hand = reinterpret_cast<float*>(smem_u8);
+    if (grp == 1) {
+#pragma unroll
+      for (int b = 0; b < TOK; ++b) hand[b * EMAX + e_own] = acc[b];
+    }
+    __syncthreads();
+    if (grp == 0) {
+#pragma unroll
+      for (int b = 0; b < TOK; ++b) acc[b] += hand[b * EMAX + e_own];
+    }
+  }
 
   // Push: token b is owned by rank b % S (local slot b / S); every rank
   // stores its partial logits of b into the owner's receive buffer at
@@ -176,19 +192,21 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   // buffer is never used for staging, so no rank can overwrite live data.
   const int slots = (TOK + static_cast<int>(S) - 1) / static_cast<int>(S);
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (grp == 0) {
 #pragma unroll
-  for (int b = 0; b < TOK; ++b) {
-    const unsigned owner = static_cast<unsigned>(b) % S;
-    float* dst = cluster.map_shared_rank(recv, owner) + (rank * slots + b / static_cast<int>(S)) * EMAX;
-#pragma unroll
-    for (int a = 0; a < EPT; ++a) dst[tid + kRouterThreads * a] = acc[a][b];
+    for (int b = 0; b < TOK; ++b) {
+      const unsigned owner = static_cast<unsigned>(b) % S;
+      float* dst = cluster.map_shared_rank(recv, owner) + (rank * slots + b / static_cast<int>(S)) * EMAX;
+      dst[e_own] = acc[b];
+    }
   }
   cluster.sync();   // every partial row has arrived at its owner
   // One warp per owned token: sum the S partial rows in rank order
   // (deterministic), add the bias, select.
+  constexpr int kWarps = kRouterThreads / 32;
   const int warp = tid >> 5, lane = tid & 31;
   float* lrow = rows + warp * EMAX;
-  for (int sl = warp; sl < slots; sl += 4) {
+  for (int sl = warp; sl < slots; sl += kWarps) {
     const int b = sl * static_cast<int>(S) + static_cast<int>(rank);
     const int t = t0 + b;
     if (b >= TOK || t >= T) break;
@@ -205,16 +223,16 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   }
 }
 
-template <typename XT, int TOK, int EPT, int NBUF>
+template <typename XT, int TOK, int EMAX>
 static cudaError_t launch_router_t(const void* x, const float* wr, const float* bias, int T, int d, int E, int k,
                                    int S, int32_t* ids, float* w, unsigned* status, cudaStream_t stream) {
-  using L = RouterSmem<XT, TOK, EPT>;
+  using L = RouterSmem<XT, TOK, EMAX>;
   const int tiles = ceil_div(T, TOK);
   // hidden-dim slice per cluster rank, a multiple of the staging chunk
   const int kslice = ceil_div(ceil_div(d, S), kRouterKC) * kRouterKC;
-  constexpr size_t smem = NBUF * L::kStage + L::kRecv + L::kRows;
+  constexpr size_t smem = L::kTotal;
   static_assert(smem <= 227 * 1024, "router staging exceeds shared memory");
-  cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(router_kernel<XT, TOK, EPT, NBUF>),
+  cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(router_kernel<XT, TOK, EMAX>),
                                         static_cast<int>(smem), S > 8);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -230,13 +248,13 @@ static cudaError_t launch_router_t(const void* x, const float* wr, const float* 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launches(1);
-  return cudaLaunchKernelEx(&cfg, router_kernel<XT, TOK, EPT, NBUF>, static_cast<const XT*>(x), wr, bias, T, d, E,
-                            k, kslice, ids, w, status);
+  return cudaLaunchKernelEx(&cfg, router_kernel<XT, TOK, EMAX>, static_cast<const XT*>(x), wr, bias, T, d, E, k,
+                            kslice, ids, w, status);
 }
 
 // Chooses tokens-per-CTA and the cluster split so that small T still spreads
 // over the SMs: S ranks split d (up to 16, a non-portable cluster size the
-// GPU supports), each rank at least one staging chunk.
+// GPU supports), each rank at least two staging chunks.
 cudaError_t launch_router(const void* x, bool x_bf16, const float* wr, const float* bias, int T, int d, int E,
                           int k, int32_t* ids, float* w, unsigned* status, int num_sms, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
@@ -244,16 +262,16 @@ cudaError_t launch_router(const void* x, bool x_bf16, const float* wr, const flo
   const int TOK = big ? 32 : 8;
   const int tiles = ceil_div(T, TOK);
   int S = 1;
-  while (S < 16 && tiles * S < num_sms && d / (2 * S) >= kRouterKC) S *= 2;
+  while (S < 16 && tiles * S < num_sms && d / (2 * S) >= 2 * kRouterKC) S *= 2;
   const bool e128 = E <= 128;
-#define MOE_ROUTER_CASE(XT, TOKC, EPT, NB) \
-  return launch_router_t<XT, TOKC, EPT, NB>(x, wr, bias, T, d, E, k, S, ids, w, status, stream)
+#define MOE_ROUTER_CASE(XT, TOKC, EM) \
+  return launch_router_t<XT, TOKC, EM>(x, wr, bias, T, d, E, k, S, ids, w, status, stream)
   if (x_bf16) {
-    if (big) { if (e128) MOE_ROUTER_CASE(uint16_t, 32, 1, 2); else MOE_ROUTER_CASE(uint16_t, 32, 2, 1); }
-    else     { if (e128) MOE_ROUTER_CASE(uint16_t, 8, 1, 2); else MOE_ROUTER_CASE(uint16_t, 8, 2, 1); }
+    if (big) { if (e128) MOE_ROUTER_CASE(uint16_t, 32, 128); else MOE_ROUTER_CASE(uint16_t, 32, 256); }
+    else     { if (e128) MOE_ROUTER_CASE(uint16_t, 8, 128); else MOE_ROUTER_CASE(uint16_t, 8, 256); }
   } else {
-    if (big) { if (e128) MOE_ROUTER_CASE(float, 32, 1, 2); else MOE_ROUTER_CASE(float, 32, 2, 1); }
-    else     { if (e128) MOE_ROUTER_CASE(float, 8, 1, 2); else MOE_ROUTER_CASE(float, 8, 2, 1); }
+    if (big) { if (e128) MOE_ROUTER_CASE(float, 32, 128); else MOE_ROUTER_CASE(float, 32, 256); }
+    else     { if (e128) MOE_ROUTER_CASE(float, 8, 128); else MOE_ROUTER_CASE(float, 8, 256); }
   }
 #undef MOE_ROUTER_CASE
 }
