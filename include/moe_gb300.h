@@ -99,6 +99,8 @@ typedef struct {
  *              (w13_scale [E][2f][d/16] ...); *_gscale = float per expert
  *              ([E] for w13/w2, one float for s13/s2);
  *              value = e2m1(code) * e4m3(block scale) * gscale.
+ * Alignment: w13 / w2 / s13 / s2 16 bytes; E4M3 row scales 4 bytes; NVFP4
+ * block-scale arrays 8 bytes (a misaligned pointer is MOE_ERR_INVALID_ARG).
  * Source of the formats: the Sarvam summary page (peacm.com news/791474,
  * section 2.1, FP8 expert weights) and the Sarvam blog's Blackwell section
  * (NVFP4 weights).

@@ -160,8 +160,9 @@ bool weights_ok(const moe_config_t& c, const moe_weights_t* w) {
     if (!aligned(p, 16)) return false;
   if (c.w_dtype == MOE_E4M3 || c.w_dtype == MOE_NVFP4) {
     const void* s[4] = {w->w13_scale, w->w2_scale, w->s13_scale, w->s2_scale};
+    const size_t a = (c.w_dtype == MOE_NVFP4) ? 8 : 4;   // NVFP4 scales are fetched 8 bytes at a time
     for (const void* p : s)
-      if (!p || !aligned(p, 4)) return false;
+      if (!p || !aligned(p, a)) return false;
   }
   if (c.w_dtype == MOE_NVFP4) {
     if (!w->w13_gscale || !w->w2_gscale || !w->s13_gscale || !w->s2_gscale) return false;

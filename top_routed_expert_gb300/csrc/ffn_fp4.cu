@@ -13,13 +13,18 @@
 // weight scale and the row scale (times the gate weight in the down
 // projection) are applied in the epilogue.
 //
-// Warp roles (320 threads): warp 0 issues the TMA loads of the activation
+// Warp roles (480 threads): warp 0 issues the TMA loads of the activation
 // tiles, warp 1 owns TMEM and issues the MMAs, warps 2-5 are the epilogue,
-// warps 6-9 convert weights.  Each converter thread owns one weight row of
-// every A tile: it streams the row's packed codes and block scales with
-// cp.async several k-blocks ahead into a private ring, converts, writes the
-// swizzled f16 row, fences the async proxy and arrives on the stage's
-// "weights ready" barrier.  Every wait is bounded (timeout -> status word).
+// warps 6-13 convert weights and warp 14 streams the raw weights.  The raw
+// stream runs well ahead of the MMA: every 128-element k-block of every
+// weight row (64 bytes of packed codes, a TMA box of 128 rows stored with the
+// 64-byte swizzle, and 8 bytes of block scales, fetched by the 32 lanes with
+// cp.async and signalled through cp.async.mbarrier.arrive) lands in a ring of
+// up to 16 slots, so that about 100 KB of weights per SM are in flight -- what
+// a decode-sized batch needs to keep HBM busy.  Converter threads turn a slot
+// into two 64-element f16 stages (one row, or half a row, per thread),
+// fence the async proxy and release the slot.  Every wait is bounded
+// (timeout -> status word).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -32,15 +37,17 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kF4Threads = 320;
+constexpr int kF4Threads = 480;
 constexpr int kF4Epi = 128;                 // warps 2-5
-constexpr int kF4Conv = 128;                // warps 6-9
-constexpr int kF4BK = 64;                   // K elements per k-block (128 bytes of f16)
+constexpr int kF4ConvWarps = 8;             // warps 6-13
+constexpr int kF4BK = 64;                   // K elements per f16 stage (128 bytes of f16)
+constexpr int kF4RK = 128;                  // K elements per raw slot (two f16 stages)
 constexpr int kF4BM = 128;                  // weight rows per tile
 constexpr uint32_t kF4ATile = kF4BM * 128;  // 16 KB f16 tile
-constexpr int kF4MaxStages = 6;
-constexpr int kF4RawSlots = 4;              // cp.async ring depth (prefetch 3 k-blocks ahead)
-constexpr int kF4RawRow = 48;               // 32 bytes of codes + 4 bytes of scales, 16-byte aligned
+constexpr uint32_t kF4RawCodes = kF4BM * (kF4RK / 2);    // 8 KB of packed codes per weight tile
+constexpr uint32_t kF4RawScales = kF4BM * (kF4RK / 16);  // 1 KB of block scales per weight tile
+constexpr int kF4MaxStages = 3;
+constexpr int kF4MaxRaw = 16;
 constexpr uint64_t kF4WaitNs = 2000000000ull;
 constexpr uint64_t kF4DrainNs = 200000000ull;
 constexpr int kF4SmemBudget = 200 * 1024;
@@ -49,10 +56,8 @@ struct F4Args {
   const int32_t* offsets;
   const int32_t* sorted_pair;
   const float* topk_w;
-  const uint8_t* wq;          // routed packed codes [E][rows][K/2]
   const uint8_t* wsc;         // routed block scales [E][rows][K/16]
   const float* wg;            // routed global scales [E]
-  const uint8_t* sq;          // shared expert codes [rows_s][K_s/2]
   const uint8_t* ssc;         // shared block scales
   const float* sg;            // shared global scale (one float)
   const float* b_scale;       // per-row activation scale [P+T]
@@ -61,14 +66,16 @@ struct F4Args {
   void* shared_out;           // gemm2 out [T][d]
   bool out_bf16;
   int T, k, E, P, d, f, fs, fmax;
-  int TN, stages, acc_bufs, tmem_cols;
+  int TN, stages, raw_slots, acc_bufs, tmem_cols;
   unsigned* status;
 };
 
 struct __align__(16) F4Ctrl {
   uint64_t full[kF4MaxStages];     // activation tile landed (TMA tx count)
-  uint64_t aready[kF4MaxStages];   // weight tiles converted (kF4Conv arrivals)
+  uint64_t aready[kF4MaxStages];   // weight tiles converted (one arrival per converter warp)
   uint64_t empty[kF4MaxStages];    // stage free again (MMA commit)
+  uint64_t rfull[kF4MaxRaw];       // raw slot landed (TMA tx count + 32 cp.async arrivals)
+  uint64_t rempty[kF4MaxRaw];      // raw slot converted (one arrival per converter warp)
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -79,19 +86,13 @@ struct __align__(16) F4Ctrl {
   GroupTable gt;
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait_keep(int keep) {
-  // wait until at most `keep` groups are pending (keep is 0..3)
-  if (keep >= 3) asm volatile("cp.async.wait_group 3;" ::: "memory");
-  else if (keep == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
-  else if (keep == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
-  else asm volatile("cp.async.wait_group 0;" ::: "memory");
+// The barrier receives one arrival once all of this thread's earlier
+// cp.async copies have landed (its expected count includes that arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // Four e2m1 pairs (one 32-bit word of packed codes, element 2i in the low
@@ -138,7 +139,7 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 }
 
 // Walks this CTA's k-block sequence (tiles blockIdx.x, +gridDim.x, ...; K/64
-// k-blocks each) -- the same order for the producer, MMA and converters.
+// k-blocks each) -- the same order for the producers, MMA and converters.
 struct KbCursor {
   int i, kb, nkb;
   Tile t;
@@ -174,35 +175,33 @@ __device__ __forceinline__ void cursor_next(KbCursor& cu, const GroupTable& gt, 
   }
 }
 
-// Global row of weight tile `a_idx` (0 = gate / down, 1 = up) for this tile.
+// Row (within its tensor map: routed or shared weights) of weight tile
+// `a_idx` (0 = gate / down, 1 = up) of this tile, and its K.
 template <int MODE>
-__device__ __forceinline__ void weight_row(const F4Args& a, const Tile& t, int a_idx, int r, const uint8_t** q,
-                                           const uint8_t** sc, int* K) {
+__device__ __forceinline__ int weight_row(const F4Args& a, const Tile& t, int a_idx, int* K) {
   const bool shr = t.g == a.E;
-  int row;
   if (MODE == 1) {
     const int width = shr ? a.fs : a.f;
-    row = (shr ? 0 : t.g * 2 * a.f) + (a_idx ? width : 0) + t.wt * kF4BM + r;
     *K = a.d;
-  } else {
-    row = (shr ? 0 : t.g * a.d) + t.wt * kF4BM + r;
-    *K = shr ? a.fs : a.f;
+    return (shr ? 0 : t.g * 2 * a.f) + (a_idx ? width : 0) + t.wt * kF4BM;
   }
-  *q = (shr ? a.sq : a.wq) + static_cast<size_t>(row) * (*K / 2);
-  *sc = (shr ? a.ssc : a.wsc) + static_cast<size_t>(row) * (*K / 16);
+  *K = shr ? a.fs : a.f;
+  return (shr ? 0 : t.g * a.d) + t.wt * kF4BM;
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kF4Threads, 1)
-ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
+ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapA,
+               const __grid_constant__ CUtensorMap mapAs, F4Args a) {
   constexpr int NA = (MODE == 1) ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int N = a.TN;                                   // one f16 column per token
   const uint32_t b_bytes = static_cast<uint32_t>(N) * 128;
   const uint32_t stage_bytes = NA * kF4ATile + ((b_bytes + 1023u) & ~1023u);
-  uint8_t* raw = smem + a.stages * stage_bytes;         // [slots][NA][128 rows][48 B]
-  F4Ctrl* c = reinterpret_cast<F4Ctrl*>(raw + kF4RawSlots * NA * kF4BM * kF4RawRow);
+  constexpr uint32_t raw_slot = NA * (kF4RawCodes + kF4RawScales);   // a multiple of 1024
+  uint8_t* raw = smem + a.stages * stage_bytes;         // [slots][NA codes | NA scales]
+  F4Ctrl* c = reinterpret_cast<F4Ctrl*>(raw + a.raw_slots * raw_slot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.E + 1;
   volatile int* abort = &c->abort;
@@ -210,8 +209,12 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_u32(&c->full[s]), 1);
-      mbar_init(smem_u32(&c->aready[s]), kF4Conv);
+      mbar_init(smem_u32(&c->aready[s]), kF4ConvWarps);
       mbar_init(smem_u32(&c->empty[s]), 1);
+    }
+    for (int s = 0; s < a.raw_slots; ++s) {
+      mbar_init(smem_u32(&c->rfull[s]), 33);
+      mbar_init(smem_u32(&c->rempty[s]), kF4ConvWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&c->tfull[b]), 1);
@@ -344,18 +347,15 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
       const int col = t.wt * kF4BM + n;
       if (MODE == 1) {
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
-        for (int c0 = 0; c0 < N; c0 += 32) {       // 32 tokens per chunk
-          float gv[32], uv[32], cf[32];
+        for (int c0 = 0; c0 < N; c0 += 16) {       // 16 tokens per chunk
+          float gv[16], uv[16];
+          tmem_ld16x2(cb + c0, cb + N + c0, gv, uv);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) cf[jj] = coef[(c0 + jj) & (kF4BM - 1)];
-          tmem_ld32x2(cb + c0, cb + N + c0, gv, uv);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
+          for (int jj = 0; jj < 16; ++jj) {
             const int j = c0 + jj;
             if (j < t.nrows) {
-              const float g = gv[jj] * cf[jj];
-              const float u = uv[jj] * cf[jj];
-              a.h[static_cast<size_t>(t.row0 + j) * a.fmax + col] = __float2bfloat16_rn(silu(g) * u);
+              const float cf = coef[j];
+              a.h[static_cast<size_t>(t.row0 + j) * a.fmax + col] = __float2bfloat16_rn(silu(gv[jj] * cf) * (uv[jj] * cf));
             }
           }
         }
@@ -363,14 +363,14 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
         void* outp = shr ? a.shared_out : a.out_perm;
         const size_t out0 = static_cast<size_t>(shr ? t.row0 - a.P : t.row0) * a.d + col;
-        for (int c0 = 0; c0 < N; c0 += 64) {       // 64 tokens per chunk
-          float d0[32], d1[32];
-          tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
+        for (int c0 = 0; c0 < N; c0 += 32) {       // 32 tokens per chunk
+          float d0[16], d1[16];
+          tmem_ld16x2(cb + c0, cb + c0 + 16, d0, d1);
 #pragma unroll
-          for (int jj = 0; jj < 64; ++jj) {
+          for (int jj = 0; jj < 32; ++jj) {
             const int j = c0 + jj;
             if (j < t.nrows) {
-              const float v = jj < 32 ? d0[jj] : d1[jj - 32];
+              const float v = jj < 16 ? d0[jj] : d1[jj - 16];
               store_out(outp, out0 + static_cast<size_t>(j) * a.d, v * coef[j], a.out_bf16);
             }
           }
@@ -383,76 +383,107 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, F4Args a) {
         aph ^= 1u;
       }
     }
-  } else {
-    // -------------------------------------------------- weight converters (warps 6..9)
-    const int r = threadIdx.x - 192;                  // weight row within the tile, 0..127
-    const uint32_t raw_base = smem_u32(raw);
-    const uint32_t raw_slot_bytes = NA * kF4BM * kF4RawRow;
-    KbCursor fetch, conv;
-    cursor_begin<MODE>(fetch, c->gt, G, total, a);
+  } else if (warp < 6 + kF4ConvWarps) {
+    // -------------------------------------------------- weight converters (warps 6..13)
+    // gate/up (two weight tiles): thread -> one row of one tile; down (one
+    // tile): two threads per row, four 16-byte f16 chunks each
+    const int ct = threadIdx.x - 192;                 // 0..255
+    const int r = ct & (kF4BM - 1);
+    const int ai = (NA == 2) ? (ct >> 7) : 0;
+    constexpr int kChunks = (NA == 2) ? 8 : 4;        // f16 chunks (8 elements) per thread and stage
+    const int c_lo = (NA == 2) ? 0 : 4 * (ct >> 7);
+    const int sw = (r >> 1) & 3;                      // 64-byte swizzle of the raw code rows
+    KbCursor conv;
     cursor_begin<MODE>(conv, c->gt, G, total, a);
-    // prologue: k-blocks 0 .. kF4RawSlots-2 in flight
-    int issued = 0;
-    for (; issued < kF4RawSlots - 1; ++issued) {
-      if (fetch.valid) {
-        const uint32_t slot = raw_base + (issued % kF4RawSlots) * raw_slot_bytes;
-        for (int ai = 0; ai < NA; ++ai) {
-          const uint8_t *q, *sc;
-          int K;
-          weight_row<MODE>(a, fetch.t, ai, r, &q, &sc, &K);
-          const uint32_t dst = slot + (ai * kF4BM + r) * kF4RawRow;
-          cp_async16(dst, q + fetch.kb * 32);
-          cp_async16(dst + 16, q + fetch.kb * 32 + 16);
-          cp_async4(dst + 32, sc + fetch.kb * 4);
-        }
-        cursor_next<MODE>(fetch, c->gt, G, total, a);
-      }
-      cp_commit();
-    }
-    int st = 0, q_idx = 0;
-    uint32_t ph = 0;
-    for (; conv.valid && !*abort; cursor_next<MODE>(conv, c->gt, G, total, a), ++q_idx) {
-      // keep the ring full: issue k-block q_idx + slots - 1
-      if (fetch.valid) {
-        const uint32_t slot = raw_base + (issued % kF4RawSlots) * raw_slot_bytes;
-        for (int ai = 0; ai < NA; ++ai) {
-          const uint8_t *q, *sc;
-          int K;
-          weight_row<MODE>(a, fetch.t, ai, r, &q, &sc, &K);
-          const uint32_t dst = slot + (ai * kF4BM + r) * kF4RawRow;
-          cp_async16(dst, q + fetch.kb * 32);
-          cp_async16(dst + 16, q + fetch.kb * 32 + 16);
-          cp_async4(dst + 32, sc + fetch.kb * 4);
-        }
-        cursor_next<MODE>(fetch, c->gt, G, total, a);
-      }
-      cp_commit();
-      ++issued;
-      cp_wait_keep(kF4RawSlots - 1);                    // this k-block's raw row has landed
+    int st = 0, rs = 0;
+    uint32_t ph = 0, rph = 0;
+    for (; conv.valid && !*abort; cursor_next<MODE>(conv, c->gt, G, total, a)) {
+      const int half = conv.kb & 1;                   // which 64 of the slot's 128 K elements
+      if (half == 0 && !mbar_wait(smem_u32(&c->rfull[rs]), rph, abort, kF4WaitNs)) break;
       if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, kF4WaitNs)) break;
-      const uint8_t* rslot = raw + (q_idx % kF4RawSlots) * raw_slot_bytes;
-      for (int ai = 0; ai < NA; ++ai) {
-        const uint8_t* src = rslot + (ai * kF4BM + r) * kF4RawRow;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(src);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(src + 16);
-        const uint32_t scw = *reinterpret_cast<const uint32_t*>(src + 32);
-        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint8_t* dst_row = smem + st * stage_bytes + ai * kF4ATile + r * 128;
+      const uint8_t* slot = raw + rs * raw_slot;
+      const uint8_t* codes = slot + ai * kF4RawCodes + r * (kF4RK / 2);
+      const uint32_t scw = *reinterpret_cast<const uint32_t*>(slot + NA * kF4RawCodes + ai * kF4RawScales +
+                                                              r * (kF4RK / 16) + half * 4);
+      uint8_t* dst_row = smem + st * stage_bytes + ai * kF4ATile + r * 128;
 #pragma unroll
-        for (int chunk = 0; chunk < 8; ++chunk) {     // 8 elements (16 bytes of f16) per chunk
-          const uint32_t s2 = e4m3_to_f16x2_bcast((scw >> (8 * (chunk >> 1))) & 0xffu);
+      for (int q = 0; q < kChunks / 4; ++q) {
+        const int lc = 2 * half + (c_lo >> 2) + q;    // logical 16-byte chunk of the 64-byte code row
+        const uint4 w4 = *reinterpret_cast<const uint4*>(codes + ((lc ^ sw) << 4));
+        const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = c_lo + 4 * q + i;            // f16 chunk (8 elements) within the stage row
+          const uint32_t s2 = e4m3_to_f16x2_bcast((scw >> (8 * (ch >> 1))) & 0xffu);
           uint32_t hv[4];
-          e2m1x8_to_f16(words[chunk], s2, hv);
-          *reinterpret_cast<uint4*>(dst_row + ((chunk ^ (r & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          e2m1x8_to_f16(words[i], s2, hv);
+          *reinterpret_cast<uint4*>(dst_row + ((ch ^ (r & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
         }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(smem_u32(&c->aready[st]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c->aready[st]));
       if (++st == a.stages) {
         st = 0;
         ph ^= 1u;
       }
+      if (half == 1) {
+        if (lane == 0) mbar_arrive(smem_u32(&c->rempty[rs]));
+        if (++rs == a.raw_slots) {
+          rs = 0;
+          rph ^= 1u;
+        }
+      }
     }
+  } else {
+    // -------------------------------------------------- raw weight stream (warp 14)
+    if (lane == 0) {
+      tma_prefetch_desc(&mapA);
+      tma_prefetch_desc(&mapAs);
+    }
+    KbCursor cu;
+    cursor_begin<MODE>(cu, c->gt, G, total, a);
+    int rs = 0;
+    uint32_t rph = 0, pending = 0, last_par = 0;
+    for (; cu.valid && !*abort; cursor_next<MODE>(cu, c->gt, G, total, a)) {
+      if (cu.kb & 1) continue;                        // one slot per two f16 stages
+      // warp-uniform decision: either every lane fills the slot or none does
+      const bool free_slot = mbar_wait(smem_u32(&c->rempty[rs]), rph ^ 1u, abort, kF4WaitNs);
+      if (!__all_sync(0xffffffffu, free_slot)) break;
+      const bool shr = cu.t.g == a.E;
+      const uint32_t slot = smem_u32(raw + rs * raw_slot);
+      const uint32_t bar = smem_u32(&c->rfull[rs]);
+      const int rb = cu.kb >> 1;                      // raw block within the row
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, NA * kF4RawCodes);
+        for (int t2 = 0; t2 < NA; ++t2) {
+          int K;
+          const int row = weight_row<MODE>(a, cu.t, t2, &K);
+          tma_load_2d(slot + t2 * kF4RawCodes, shr ? &mapAs : &mapA, rb * (kF4RK / 2), row, bar);
+        }
+      }
+      for (int t2 = 0; t2 < NA; ++t2) {
+        int K;
+        const int row = weight_row<MODE>(a, cu.t, t2, &K);
+        const uint8_t* sc = (shr ? a.ssc : a.wsc) + static_cast<size_t>(row) * (K / 16) + rb * (kF4RK / 16);
+#pragma unroll
+        for (int j = 0; j < kF4BM / 32; ++j) {
+          const int rr = lane + 32 * j;
+          cp_async8(slot + NA * kF4RawCodes + t2 * kF4RawScales + rr * (kF4RK / 16),
+                    sc + static_cast<size_t>(rr) * (K / 16));
+        }
+      }
+      cp_async_arrive_noinc(bar);
+      pending |= 1u << rs;
+      last_par = (last_par & ~(1u << rs)) | (rph << rs);
+      if (++rs == a.raw_slots) {
+        rs = 0;
+        rph ^= 1u;
+      }
+    }
+    int no_abort = 0;
+    for (int s = 0; s < a.raw_slots; ++s)
+      if (pending & (1u << s)) mbar_wait(smem_u32(&c->rfull[s]), (last_par >> s) & 1u, &no_abort, kF4DrainNs);
     asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
@@ -583,6 +614,20 @@ bool make_f16_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed e2m1 codes [rows][K/2] bytes: box of 64 bytes (128 elements) x 128
+// rows, stored with the 64-byte swizzle.
+bool make_code_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+  EncodeTiledFn fn = f4_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {K / 2, rows};
+  cuuint64_t strides[1] = {K / 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kF4RK / 2), static_cast<cuuint32_t>(kF4BM)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct F4Plan {
   size_t xh, sx, h, hh, sh, total;
   int TN;
@@ -606,22 +651,28 @@ F4Plan f4_plan(const moe_config_t& c) {
 }
 
 template <int MODE>
-cudaError_t launch_f4_gemm(const CUtensorMap& mB, F4Args a, int wtiles_max, int num_sms, cudaStream_t stream) {
+cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const CUtensorMap& mAs, F4Args a,
+                           int wtiles_max, int num_sms, cudaStream_t stream) {
   constexpr int NA = (MODE == 1) ? 2 : 1;
   const int N = a.TN;
   const int stage_bytes = NA * kF4ATile + align_up(static_cast<size_t>(N) * 128, 1024);
-  const int raw_bytes = kF4RawSlots * NA * kF4BM * kF4RawRow;
-  a.stages = std::min(kF4MaxStages, (kF4SmemBudget - raw_bytes) / stage_bytes);
+  const int raw_slot = NA * (kF4RawCodes + kF4RawScales);
+  // two f16 stages suffice for narrow token tiles (the MMA is short); the
+  // rest of the budget goes to the raw ring, which hides HBM latency
+  a.stages = (N <= 32) ? 2 : kF4MaxStages;
+  a.raw_slots = std::min(kF4MaxRaw, (kF4SmemBudget - a.stages * stage_bytes) / raw_slot);
+  if (a.raw_slots < 2) return cudaErrorInvalidConfiguration;
   const int per_acc = NA * N;
   a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
-  // epilogue loads: gemm1 32 columns at c0 and N + c0; gemm2 64 columns at c0
+  // epilogue loads: gemm1 16 columns at c0 and N + c0; gemm2 32 columns at c0
   const int last = (a.acc_bufs - 1) * per_acc;
-  const int reach = (MODE == 1) ? last + N + (N + 31) / 32 * 32 : last + (N + 63) / 64 * 64;
+  const int reach = (MODE == 1) ? last + N + (N + 15) / 16 * 16 : last + (N + 31) / 32 * 32;
   int cols = 32;
   while (cols < reach) cols *= 2;
-  if (cols > 512 || a.stages < 2) return cudaErrorInvalidConfiguration;
+  if (cols > 512) return cudaErrorInvalidConfiguration;
   a.tmem_cols = cols;
-  size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + raw_bytes + sizeof(F4Ctrl);
+  size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + static_cast<size_t>(a.raw_slots) * raw_slot +
+                sizeof(F4Ctrl);
   smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
   cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_fp4_kernel<MODE>), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -629,7 +680,7 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, F4Args a, int wtiles_max, int 
       static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
   count_launches(1);
-  ffn_fp4_kernel<MODE><<<grid, kF4Threads, smem, stream>>>(mB, a);
+  ffn_fp4_kernel<MODE><<<grid, kF4Threads, smem, stream>>>(mB, mA, mAs, a);
   return cudaGetLastError();
 }
 
@@ -676,13 +727,16 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
   a.TN = pl.TN; a.status = status;
 
-  CUtensorMap mB;
+  CUtensorMap mB, mA, mAs;
   // gemm1: gate / up
-  if (!make_f16_map(&mB, xh, R, d, d, pl.TN)) return cudaErrorInvalidValue;
-  a.wq = static_cast<const uint8_t*>(w->w13); a.wsc = static_cast<const uint8_t*>(w->w13_scale); a.wg = w->w13_gscale;
-  a.sq = static_cast<const uint8_t*>(w->s13); a.ssc = static_cast<const uint8_t*>(w->s13_scale); a.sg = w->s13_gscale;
+  if (!make_f16_map(&mB, xh, R, d, d, pl.TN) ||
+      !make_code_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d) ||
+      !make_code_map(&mAs, w->s13, 2 * static_cast<uint64_t>(fs), d))
+    return cudaErrorInvalidValue;
+  a.wsc = static_cast<const uint8_t*>(w->w13_scale); a.wg = w->w13_gscale;
+  a.ssc = static_cast<const uint8_t*>(w->s13_scale); a.sg = w->s13_gscale;
   a.b_scale = sx;
-  err = launch_f4_gemm<1>(mB, a, fmax / kF4BM, num_sms, stream);
+  err = launch_f4_gemm<1>(mB, mA, mAs, a, fmax / kF4BM, num_sms, stream);
   if (err != cudaSuccess) return err;
 
   count_launches(1);
@@ -696,11 +750,14 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs
-  if (!make_f16_map(&mB, hh, R, fmax, fmax, pl.TN)) return cudaErrorInvalidValue;
-  a.wq = static_cast<const uint8_t*>(w->w2); a.wsc = static_cast<const uint8_t*>(w->w2_scale); a.wg = w->w2_gscale;
-  a.sq = static_cast<const uint8_t*>(w->s2); a.ssc = static_cast<const uint8_t*>(w->s2_scale); a.sg = w->s2_gscale;
+  if (!make_f16_map(&mB, hh, R, fmax, fmax, pl.TN) ||
+      !make_code_map(&mA, w->w2, static_cast<uint64_t>(E) * d, f) ||
+      !make_code_map(&mAs, w->s2, static_cast<uint64_t>(d), fs))
+    return cudaErrorInvalidValue;
+  a.wsc = static_cast<const uint8_t*>(w->w2_scale); a.wg = w->w2_gscale;
+  a.ssc = static_cast<const uint8_t*>(w->s2_scale); a.sg = w->s2_gscale;
   a.b_scale = sh;
-  return launch_f4_gemm<2>(mB, a, d / kF4BM, num_sms, stream);
+  return launch_f4_gemm<2>(mB, mA, mAs, a, d / kF4BM, num_sms, stream);
 }
 
 }  // namespace moe
