@@ -14,7 +14,9 @@
 // projection) are applied in the epilogue.
 //
 // Warp roles (480 threads): warp 0 issues the TMA loads of the activation
-// tiles, warp 1 owns TMEM and issues the MMAs, warps 2-5 are the epilogue,
+// tiles into a ring of their own (up to 8 slots, so that the small decode
+// tiles are fetched well ahead of the MMA), warp 1 owns TMEM and issues the
+// MMAs, warps 2-5 are the epilogue,
 // warps 6-13 convert weights and warp 14 streams the raw weights.  The raw
 // stream runs well ahead of the MMA: every 128-element k-block of every
 // weight row (64 bytes of packed codes, a TMA box of 128 rows stored with the
@@ -47,10 +49,12 @@ constexpr uint32_t kF4ATile = kF4BM * 128;  // 16 KB f16 tile
 constexpr uint32_t kF4RawCodes = kF4BM * (kF4RK / 2);    // 8 KB of packed codes per weight tile
 constexpr uint32_t kF4RawScales = kF4BM * (kF4RK / 16);  // 1 KB of block scales per weight tile
 constexpr int kF4MaxStages = 3;
+constexpr int kF4MaxB = 8;
 constexpr int kF4MaxRaw = 16;
 constexpr uint64_t kF4WaitNs = 2000000000ull;
 constexpr uint64_t kF4DrainNs = 200000000ull;
-constexpr int kF4SmemBudget = 200 * 1024;
+constexpr unsigned kF4IdleSleepNs = 128;    // poll interval of the waits that are off the critical path
+constexpr int kF4SmemBudget = 214 * 1024;
 
 struct F4Args {
   const int32_t* offsets;
@@ -66,14 +70,15 @@ struct F4Args {
   void* shared_out;           // gemm2 out [T][d]
   bool out_bf16;
   int T, k, E, P, d, f, fs, fmax;
-  int TN, stages, raw_slots, acc_bufs, tmem_cols;
+  int TN, stages, bslots, raw_slots, acc_bufs, tmem_cols;
   unsigned* status;
 };
 
 struct __align__(16) F4Ctrl {
-  uint64_t full[kF4MaxStages];     // activation tile landed (TMA tx count)
   uint64_t aready[kF4MaxStages];   // weight tiles converted (one arrival per converter warp)
-  uint64_t empty[kF4MaxStages];    // stage free again (MMA commit)
+  uint64_t empty[kF4MaxStages];    // weight stage free again (MMA commit)
+  uint64_t bfull[kF4MaxB];         // activation tile landed (TMA tx count)
+  uint64_t bempty[kF4MaxB];        // activation slot free again (MMA commit)
   uint64_t rfull[kF4MaxRaw];       // raw slot landed (TMA tx count + 32 cp.async arrivals)
   uint64_t rempty[kF4MaxRaw];      // raw slot converted (one arrival per converter warp)
   uint64_t tfull[2];
@@ -198,9 +203,11 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int N = a.TN;                                   // one f16 column per token
   const uint32_t b_bytes = static_cast<uint32_t>(N) * 128;
-  const uint32_t stage_bytes = NA * kF4ATile + ((b_bytes + 1023u) & ~1023u);
+  constexpr uint32_t stage_bytes = NA * kF4ATile;
+  const uint32_t b_slot = (b_bytes + 1023u) & ~1023u;
   constexpr uint32_t raw_slot = NA * (kF4RawCodes + kF4RawScales);   // a multiple of 1024
-  uint8_t* raw = smem + a.stages * stage_bytes;         // [slots][NA codes | NA scales]
+  uint8_t* bring = smem + a.stages * stage_bytes;       // [bslots][N rows x 128 bytes]
+  uint8_t* raw = bring + a.bslots * b_slot;             // [slots][NA codes | NA scales]
   F4Ctrl* c = reinterpret_cast<F4Ctrl*>(raw + a.raw_slots * raw_slot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.E + 1;
@@ -208,9 +215,12 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
-      mbar_init(smem_u32(&c->full[s]), 1);
       mbar_init(smem_u32(&c->aready[s]), kF4ConvWarps);
       mbar_init(smem_u32(&c->empty[s]), 1);
+    }
+    for (int s = 0; s < a.bslots; ++s) {
+      mbar_init(smem_u32(&c->bfull[s]), 1);
+      mbar_init(smem_u32(&c->bempty[s]), 1);
     }
     for (int s = 0; s < a.raw_slots; ++s) {
       mbar_init(smem_u32(&c->rfull[s]), 33);
@@ -246,27 +256,27 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
       KbCursor cu;
       cursor_begin<MODE>(cu, c->gt, G, total, a);
       for (; cu.valid && !*abort; cursor_next<MODE>(cu, c->gt, G, total, a)) {
-        if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, kF4WaitNs)) break;
-        const uint32_t full = smem_u32(&c->full[st]);
+        if (!mbar_wait_sleep(smem_u32(&c->bempty[st]), ph ^ 1u, abort, kF4WaitNs, kF4IdleSleepNs)) break;
+        const uint32_t full = smem_u32(&c->bfull[st]);
         mbar_arrive_expect_tx(full, b_bytes);
-        tma_load_2d(smem_u32(smem + st * stage_bytes + NA * kF4ATile), &mapB, cu.kb * kF4BK, cu.t.row0, full);
+        tma_load_2d(smem_u32(bring + st * b_slot), &mapB, cu.kb * kF4BK, cu.t.row0, full);
         pending |= 1u << st;
         last_par = (last_par & ~(1u << st)) | (ph << st);
-        if (++st == a.stages) {
+        if (++st == a.bslots) {
           st = 0;
           ph ^= 1u;
         }
       }
       int no_abort = 0;
-      for (int s = 0; s < a.stages; ++s)
-        if (pending & (1u << s)) mbar_wait(smem_u32(&c->full[s]), (last_par >> s) & 1u, &no_abort, kF4DrainNs);
+      for (int s = 0; s < a.bslots; ++s)
+        if (pending & (1u << s)) mbar_wait(smem_u32(&c->bfull[s]), (last_par >> s) & 1u, &no_abort, kF4DrainNs);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       const uint32_t idesc = idesc_f16(kF4BM, N);
-      int st = 0, ab = 0;
-      uint32_t ph = 0, aph = 0;
+      int st = 0, bs = 0, ab = 0;
+      uint32_t ph = 0, bph = 0, aph = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
         const Tile t = decode_tile(c->gt, G, i, a.TN);
@@ -276,7 +286,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
         const uint32_t d0 = tmem + static_cast<uint32_t>(ab * NA * N);
         const uint32_t d1 = d0 + static_cast<uint32_t>(N);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(smem_u32(&c->full[st]), ph, abort, kF4WaitNs) ||
+          if (!mbar_wait(smem_u32(&c->bfull[bs]), bph, abort, kF4WaitNs) ||
               !mbar_wait(smem_u32(&c->aready[st]), ph, abort, kF4WaitNs)) {
             ok = false;
             break;
@@ -285,7 +295,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
           const uint32_t sA = smem_u32(smem + st * stage_bytes);
           const uint64_t da0 = desc_sw128(sA);
           const uint64_t da1 = desc_sw128(sA + kF4ATile);
-          const uint64_t db = desc_sw128(sA + NA * kF4ATile);
+          const uint64_t db = desc_sw128(smem_u32(bring + bs * b_slot));
 #pragma unroll
           for (int kk = 0; kk < kF4BK / 16; ++kk) {
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
@@ -293,9 +303,14 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
             if (MODE == 1) mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum);
           }
           mma_commit(smem_u32(&c->empty[st]));
+          mma_commit(smem_u32(&c->bempty[bs]));
           if (++st == a.stages) {
             st = 0;
             ph ^= 1u;
+          }
+          if (++bs == a.bslots) {
+            bs = 0;
+            bph ^= 1u;
           }
         }
         if (!ok) break;
@@ -338,11 +353,11 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
         c->coef[cb_par][et] = cf;
       }
       mbar_arrive(smem_u32(&c->ep_sync));
-      if (!mbar_wait(smem_u32(&c->ep_sync), eph, abort, kF4WaitNs)) break;
+      if (!mbar_wait_sleep(smem_u32(&c->ep_sync), eph, abort, kF4WaitNs, kF4IdleSleepNs)) break;
       eph ^= 1u;
       const float* coef = c->coef[cb_par];
       cb_par ^= 1;
-      if (!mbar_wait(smem_u32(&c->tfull[ab]), aph, abort, kF4WaitNs)) break;
+      if (!mbar_wait_sleep(smem_u32(&c->tfull[ab]), aph, abort, kF4WaitNs, kF4IdleSleepNs)) break;
       tc_fence_after();
       const int col = t.wt * kF4BM + n;
       if (MODE == 1) {
@@ -448,7 +463,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
     for (; cu.valid && !*abort; cursor_next<MODE>(cu, c->gt, G, total, a)) {
       if (cu.kb & 1) continue;                        // one slot per two f16 stages
       // warp-uniform decision: either every lane fills the slot or none does
-      const bool free_slot = mbar_wait(smem_u32(&c->rempty[rs]), rph ^ 1u, abort, kF4WaitNs);
+      const bool free_slot = mbar_wait_sleep(smem_u32(&c->rempty[rs]), rph ^ 1u, abort, kF4WaitNs, kF4IdleSleepNs);
       if (!__all_sync(0xffffffffu, free_slot)) break;
       const bool shr = cu.t.g == a.E;
       const uint32_t slot = smem_u32(raw + rs * raw_slot);
@@ -655,12 +670,15 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
                            int wtiles_max, int num_sms, cudaStream_t stream) {
   constexpr int NA = (MODE == 1) ? 2 : 1;
   const int N = a.TN;
-  const int stage_bytes = NA * kF4ATile + align_up(static_cast<size_t>(N) * 128, 1024);
+  const int stage_bytes = NA * kF4ATile;
+  const int b_slot = static_cast<int>(align_up(static_cast<size_t>(N) * 128, 1024));
   const int raw_slot = NA * (kF4RawCodes + kF4RawScales);
-  // two f16 stages suffice for narrow token tiles (the MMA is short); the
-  // rest of the budget goes to the raw ring, which hides HBM latency
-  a.stages = (N <= 32) ? 2 : kF4MaxStages;
-  a.raw_slots = std::min(kF4MaxRaw, (kF4SmemBudget - a.stages * stage_bytes) / raw_slot);
+  // three f16 weight stages; activation slots for about 32 KB (at least 3,
+  // at most 8); the rest of the budget goes to the raw ring, which hides HBM
+  // latency
+  a.stages = kF4MaxStages;
+  a.bslots = std::max(3, std::min(kF4MaxB, 32768 / b_slot));
+  a.raw_slots = std::min(kF4MaxRaw, (kF4SmemBudget - a.stages * stage_bytes - a.bslots * b_slot) / raw_slot);
   if (a.raw_slots < 2) return cudaErrorInvalidConfiguration;
   const int per_acc = NA * N;
   a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
@@ -671,9 +689,10 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
   while (cols < reach) cols *= 2;
   if (cols > 512) return cudaErrorInvalidConfiguration;
   a.tmem_cols = cols;
-  size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + static_cast<size_t>(a.raw_slots) * raw_slot +
-                sizeof(F4Ctrl);
+  size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + static_cast<size_t>(a.bslots) * b_slot +
+                static_cast<size_t>(a.raw_slots) * raw_slot + sizeof(F4Ctrl);
   smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
+  if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_fp4_kernel<MODE>), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const long long tiles_ub =
