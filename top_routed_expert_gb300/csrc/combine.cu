@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const IT* __restrict__ out_perm, const int32_t* __restrict__ row_of,
                const IT* __restrict__ shared, void* __restrict__ y, int T, int d, int k, int P,
                unsigned* status) {
+  pdl_enter();
   const int d4 = d / 4;
   const size_t total = static_cast<size_t>(T) * d4;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
@@ -58,13 +59,14 @@ cudaError_t launch_combine(const void* out_perm, const int32_t* row_of, const vo
   if (in_bf16) {
     const BF* o = static_cast<const BF*>(out_perm);
     const BF* sh = static_cast<const BF*>(shared);
-    if (y_bf16) combine_kernel<BF, true><<<blocks, 256, 0, stream>>>(o, row_of, sh, y, T, d, k, T * k, status);
-    else combine_kernel<BF, false><<<blocks, 256, 0, stream>>>(o, row_of, sh, y, T, d, k, T * k, status);
+    if (y_bf16) return launch_pdl(combine_kernel<BF, true>, blocks, 256, 0, stream, o, row_of, sh, y, T, d, k, T * k, status);
+    return launch_pdl(combine_kernel<BF, false>, blocks, 256, 0, stream, o, row_of, sh, y, T, d, k, T * k, status);
   } else {
     const float* o = static_cast<const float*>(out_perm);
     const float* sh = static_cast<const float*>(shared);
-    if (y_bf16) combine_kernel<float, true><<<blocks, 256, 0, stream>>>(o, row_of, sh, y, T, d, k, T * k, status);
-    else combine_kernel<float, false><<<blocks, 256, 0, stream>>>(o, row_of, sh, y, T, d, k, T * k, status);
+    if (y_bf16)
+      return launch_pdl(combine_kernel<float, true>, blocks, 256, 0, stream, o, row_of, sh, y, T, d, k, T * k, status);
+    return launch_pdl(combine_kernel<float, false>, blocks, 256, 0, stream, o, row_of, sh, y, T, d, k, T * k, status);
   }
   return cudaGetLastError();
 }

@@ -16,6 +16,39 @@
 
 namespace moe {
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialization, so it may be scheduled while the
+// previous kernel in the stream is still finishing.  Each kernel therefore
+// calls pdl_wait() before it touches global memory that earlier work writes
+// or reads (it returns once the previous kernel has completed and its writes
+// are visible), and then pdl_launch_dependents() to let the next kernel be
+// scheduled early.  A kernel launched without the attribute returns from
+// pdl_wait() at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
+// Launch with programmatic stream serialization (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+
 constexpr int kMaxExperts = 256;
 constexpr int kMaxGroups = kMaxExperts + 1;   // routed experts + the shared expert
 

@@ -235,6 +235,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
     c->abort = 0;
     fence_barrier_init();
   }
+  pdl_enter();   // from here on the kernel reads what earlier kernels wrote
   if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kF4BM, a.fs / kF4BM, a.status);
   else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kF4BM, a.d / kF4BM, a.status);
   if (warp == 1) {
@@ -519,6 +520,7 @@ __global__ void __launch_bounds__(256)
 scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                     int width_r, int width_s, int src_stride, __half* __restrict__ dst, int dst_stride,
                     float* __restrict__ scale, unsigned* status) {
+  pdl_enter();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= P + T) return;
@@ -699,8 +701,7 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
       static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
   count_launches(1);
-  ffn_fp4_kernel<MODE><<<grid, kF4Threads, smem, stream>>>(mB, mA, mAs, a);
-  return cudaGetLastError();
+  return launch_pdl(ffn_fp4_kernel<MODE>, grid, kF4Threads, smem, stream, mB, mA, mAs, a);
 }
 
 }  // namespace
@@ -730,13 +731,9 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   const int qblocks = ceil_div(R, 8);
   const bool regs = R <= 4096;   // see the FP8 path: registers for few rows, two passes for many
   count_launches(1);
-  if (regs)
-    scale16_rows_kernel<true, true><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T,
-                                                                 k, d, d, d, xh, d, sx, status);
-  else
-    scale16_rows_kernel<true, false><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T,
-                                                                  k, d, d, d, xh, d, sx, status);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(regs ? scale16_rows_kernel<true, true> : scale16_rows_kernel<true, false>, qblocks, 256,
+                               0, stream, static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d, d, d, xh, d, sx,
+                               status);
   if (err != cudaSuccess) return err;
 
   F4Args a = {};
@@ -759,13 +756,9 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   if (err != cudaSuccess) return err;
 
   count_launches(1);
-  if (regs)
-    scale16_rows_kernel<false, true><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P, T,
-                                                                  k, f, fs, fmax, hh, fmax, sh, status);
-  else
-    scale16_rows_kernel<false, false><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P,
-                                                                   T, k, f, fs, fmax, hh, fmax, sh, status);
-  err = cudaGetLastError();
+  err = launch_pdl(regs ? scale16_rows_kernel<false, true> : scale16_rows_kernel<false, false>, qblocks, 256, 0,
+                   stream, reinterpret_cast<const uint16_t*>(h), static_cast<const int32_t*>(nullptr), P, T, k, f, fs,
+                   fmax, hh, fmax, sh, status);
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs

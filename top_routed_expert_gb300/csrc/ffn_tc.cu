@@ -118,6 +118,9 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     c->abort = 0;
     fence_barrier_init();
   }
+  // everything above overlaps the previous kernel's tail; from here on the
+  // kernel reads what earlier kernels wrote
+  pdl_enter();
   // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
   if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kBM, a.fs / kBM, a.status);
   else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kBM, a.d / kBM, a.status);
@@ -345,6 +348,7 @@ __global__ void __launch_bounds__(256)
 quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                    int width_r, int width_s, int src_stride, uint8_t* __restrict__ q, int q_stride,
                    float* __restrict__ scale, unsigned* status) {
+  pdl_enter();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= P + T) return;
@@ -528,8 +532,7 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUt
       static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
   count_launches(1);
-  ffn_tc_kernel<MODE><<<grid, kTcThreads, smem, stream>>>(mA, mAS, mB, a);
-  return cudaGetLastError();
+  return launch_pdl(ffn_tc_kernel<MODE>, grid, kTcThreads, smem, stream, mA, mAS, mB, a);
 }
 
 }  // namespace
@@ -561,13 +564,9 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   const int qblocks = ceil_div(R, 8);
   const bool regs = R <= 4096;
   count_launches(1);
-  if (regs)
-    quant2_rows_kernel<true, true><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T, k,
-                                                                d, d, d, xq, d, sx, status);
-  else
-    quant2_rows_kernel<true, false><<<qblocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), sorted_pair, P, T,
-                                                                 k, d, d, d, xq, d, sx, status);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(regs ? quant2_rows_kernel<true, true> : quant2_rows_kernel<true, false>, qblocks, 256, 0,
+                               stream, static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d, d, d, xq, d, sx,
+                               status);
   if (err != cudaSuccess) return err;
 
   CUtensorMap mA, mAS, mB;
@@ -594,13 +593,9 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   if (err != cudaSuccess) return err;
 
   count_launches(1);
-  if (regs)
-    quant2_rows_kernel<false, true><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P, T,
-                                                                 k, f, fs, fmax, hq, fmax, sh, status);
-  else
-    quant2_rows_kernel<false, false><<<qblocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(h), nullptr, P,
-                                                                  T, k, f, fs, fmax, hq, fmax, sh, status);
-  err = cudaGetLastError();
+  err = launch_pdl(regs ? quant2_rows_kernel<false, true> : quant2_rows_kernel<false, false>, qblocks, 256, 0, stream,
+                   reinterpret_cast<const uint16_t*>(h), static_cast<const int32_t*>(nullptr), P, T, k, f, fs, fmax,
+                   hq, fmax, sh, status);
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs

@@ -26,6 +26,7 @@ constexpr int kPermMaxE = 256;
 __global__ void __launch_bounds__(kPermThreads)
 permute_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ blk_counts,
                     unsigned* status) {
+  pdl_enter();
   __shared__ int hist[kPermMaxE];
   for (int e = threadIdx.x; e < E; e += kPermThreads) hist[e] = 0;
   __syncthreads();
@@ -44,6 +45,7 @@ permute_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __re
 __global__ void __launch_bounds__(kPermThreads)
 permute_scan_kernel(const int32_t* __restrict__ blk_counts, int nblk, int E, int P,
                     int32_t* __restrict__ offsets, int32_t* __restrict__ blk_base) {
+  pdl_enter();
   __shared__ int tot[kPermMaxE];
   __shared__ int off[kPermMaxE + 1];
   const int e = threadIdx.x;
@@ -73,6 +75,7 @@ permute_scan_kernel(const int32_t* __restrict__ blk_counts, int nblk, int E, int
 __global__ void __launch_bounds__(kPermThreads)
 permute_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int32_t* __restrict__ blk_base,
                        int32_t* __restrict__ sorted_pair, int32_t* __restrict__ row_of) {
+  pdl_enter();
   constexpr int W = kPermThreads / 32;
   __shared__ int run[kPermMaxE];        // next free position per expert for this CTA
   __shared__ int wcnt[W][kPermMaxE];    // pairs per (warp, expert) in the current sub-chunk
@@ -115,6 +118,7 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int3
 __global__ void __launch_bounds__(kPermThreads)
 permute_small_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ offsets,
                      int32_t* __restrict__ sorted_pair, int32_t* __restrict__ row_of, unsigned* status) {
+  pdl_enter();
   constexpr int W = kPermThreads / 32;
   __shared__ int run[kPermMaxE + 1];
   __shared__ int wcnt[W][kPermMaxE];
@@ -183,14 +187,17 @@ cudaError_t launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, i
   }
   if (nblk == 1) {
     count_launches(1);
-    permute_small_kernel<<<1, kPermThreads, 0, stream>>>(ids, P, E, offsets, sorted_pair, row_of, status);
-    return cudaGetLastError();
+    return launch_pdl(permute_small_kernel, 1, kPermThreads, 0, stream, ids, P, E, offsets, sorted_pair, row_of,
+                      status);
   }
   count_launches(3);
-  permute_hist_kernel<<<nblk, kPermThreads, 0, stream>>>(ids, P, E, blk_counts, status);
-  permute_scan_kernel<<<1, kPermThreads, 0, stream>>>(blk_counts, nblk, E, P, offsets, blk_base);
-  permute_scatter_kernel<<<nblk, kPermThreads, 0, stream>>>(ids, P, E, blk_base, sorted_pair, row_of);
-  return cudaGetLastError();
+  cudaError_t err = launch_pdl(permute_hist_kernel, nblk, kPermThreads, 0, stream, ids, P, E, blk_counts, status);
+  if (err == cudaSuccess)
+    err = launch_pdl(permute_scan_kernel, 1, kPermThreads, 0, stream, blk_counts, nblk, E, P, offsets, blk_base);
+  if (err == cudaSuccess)
+    err = launch_pdl(permute_scatter_kernel, nblk, kPermThreads, 0, stream, ids, P, E, blk_base, sorted_pair,
+                     row_of);
+  return err;
 }
 
 // ---------------------------------------------------------------------------

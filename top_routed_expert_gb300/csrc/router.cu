@@ -113,6 +113,7 @@ router_kernel(const XT* __restrict__ x, const float* __restrict__ wr, const floa
   const int kend = min(d, kbeg + kslice);
   const int nchunks = (kend - kbeg) / kRouterKC;
 
+  pdl_enter();
   // distributed shared memory may only be touched once every CTA of the
   // cluster runs: arrive now, wait before the first remote store
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -240,13 +241,15 @@ static cudaError_t launch_router_t(const void* x, const float* wr, const float* 
   cfg.blockDim = dim3(kRouterThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   count_launches(1);
   return cudaLaunchKernelEx(&cfg, router_kernel<XT, TOK, EMAX>, static_cast<const XT*>(x), wr, bias, T, d, E, k,
                             kslice, ids, w, status);

@@ -69,6 +69,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
 
 // W_r [E][d] fp32 -> planes [3][128][d] bf16 (rows >= E are zero).
 __global__ void router_split_kernel(const float* __restrict__ wr, int E, int d, __nv_bfloat16* __restrict__ w3) {
+  pdl_enter();
   const size_t plane = static_cast<size_t>(kRtRows) * d;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < plane;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -108,6 +109,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant
     c->abort = 0;
     fence_barrier_init();
   }
+  pdl_enter();   // from here on the kernel reads what earlier kernels wrote
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), kRtTok);
     tmem_relinquish();
@@ -258,8 +260,7 @@ cudaError_t launch_router_tc(const void* x, const float* wr, const float* bias, 
   __nv_bfloat16* w3 = static_cast<__nv_bfloat16*>(ws);
   const int split_blocks = std::min(ceil_div(kRtRows * d, 256), 8 * num_sms);
   count_launches(1);
-  router_split_kernel<<<split_blocks, 256, 0, stream>>>(wr, E, d, w3);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(router_split_kernel, split_blocks, 256, 0, stream, wr, E, d, w3);
   if (err != cudaSuccess) return err;
   CUtensorMap mW, mX;
   if (!make_bf16_map(&mW, w3, 3 * static_cast<uint64_t>(kRtRows), d, kRtRows) ||
@@ -271,8 +272,8 @@ cudaError_t launch_router_tc(const void* x, const float* wr, const float* bias, 
   err = ensure_kernel_attrs(reinterpret_cast<const void*>(router_tc_kernel), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   count_launches(1);
-  router_tc_kernel<<<ceil_div(T, kRtTok), kRtThreads, smem, stream>>>(mW, mX, bias, T, d, E, k, ids, w, status);
-  return cudaGetLastError();
+  return launch_pdl(router_tc_kernel, ceil_div(T, kRtTok), kRtThreads, smem, stream, mW, mX, bias, T, d, E, k, ids, w,
+                    status);
 }
 
 }  // namespace moe
