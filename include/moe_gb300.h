@@ -63,6 +63,19 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtyp
 #define MOE_FLAG_SIMT_FFN 0x1u     /* run the expert FFN on the CUDA-core kernels */
 #define MOE_FLAG_SIMT_ROUTER 0x2u  /* run the router on the CUDA-core kernel       */
 #define MOE_FLAG_BF16_EXPERT_OUT 0x4u  /* out_perm / shared_out in bf16 (default fp32) */
+/* 8-bit activations (opt-in, lossy).  By default the FP8 expert GEMMs feed each
+ * activation row (x, and H after SwiGLU) to the tensor cores as two E4M3 terms
+ * under a per-row power-of-two scale, which reproduces bf16 activations
+ * exactly; with this flag only the first term is kept: the row is scaled by
+ * s = the smallest power of two with amax <= 448 s, rounded to E4M3 (nearest,
+ * ties to even) and H is rounded to bf16 before that.  The MMAs then do half
+ * the work.  Error against exact activations is about 5e-2 relative L2 (the
+ * E4M3 rounding of every activation), so this is a different numerical
+ * contract from the default.  Valid only with E4M3 weights, bf16 x, widths
+ * that are multiples of 128 and without MOE_FLAG_SIMT_FFN.  The pages fix the
+ * weight formats only; this is the 8-bit-activation reading of their FP8
+ * compute. */
+#define MOE_FLAG_ACT_E4M3 0x8u
 /* Test hook for the failure path: in the tensor-core expert GEMM, CTA 0
  * withholds one "accumulator ready" signal and every bounded wait shortens to
  * 20 ms, so the epilogue's wait runs out; the kernel drains its copies and

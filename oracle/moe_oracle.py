@@ -196,6 +196,65 @@ def permute(ids: np.ndarray, E: int):
 
 
 # --------------------------------------------------------------------------
+# Optional 8-bit activations.  The default layer uses the activations as
+# they are.  The opt-in lossy mode of the library (one E4M3 term per
+# activation row) is checked against this restatement of its rounding:
+#   row scale  s = the smallest power of two (>= 2^-126) with max|v| <= 448 s
+#              (1 for a row without a non-zero finite maximum);
+#   value      s * E4M3(v / s), E4M3 = nearest value, ties to the even code;
+#   H          rounded to fp32, then to bf16 (nearest even) before that.
+# The pages fix only the weight formats; this is the 8-bit-activation
+# reading of their FP8 compute, listed with the other readings.
+# --------------------------------------------------------------------------
+
+# finite non-negative E4M3 values, code 0 .. 126 (ascending with the code)
+_E4M3_POS = np.array([_e4m3_value(c) for c in range(0x7F)], dtype=np.float64)
+
+
+def encode_e4m3(v: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 value of each element, ties to the even code, saturating
+    at +-448 (returns the values, not the codes)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    i = np.clip(np.searchsorted(_E4M3_POS, a, side="right") - 1, 0, 125)   # value(i) <= a < value(i+1)
+    lo, hi = _E4M3_POS[i], _E4M3_POS[i + 1]
+    up = (a - lo > hi - a) | ((a - lo == hi - a) & ((i & 1) == 1))
+    code = np.where(up, i + 1, i)
+    code = np.where(a >= _E4M3_POS[126], 126, code)
+    return np.sign(v) * _E4M3_POS[code]
+
+
+def act_scale(amax: float) -> float:
+    """The smallest power of two s >= 2^-126 with amax <= 448 s."""
+    if not (amax > 0.0) or not math.isfinite(amax):
+        return 1.0
+    k = max(math.ceil(math.log2(amax / 448.0)), -126)
+    while k > -126 and amax <= 448.0 * 2.0 ** (k - 1):   # exact comparisons settle the log's rounding
+        k -= 1
+    while amax > 448.0 * 2.0 ** k:
+        k += 1
+    return 2.0 ** k
+
+
+def quantize_act_rows(V: np.ndarray) -> np.ndarray:
+    """Each row v -> s * E4M3(v / s) with its own scale s = act_scale(max|v|)."""
+    V = np.asarray(V, dtype=np.float64)
+    out = np.empty_like(V)
+    for r in range(V.shape[0]):
+        s = act_scale(float(np.max(np.abs(V[r]))) if V.shape[1] else 0.0)
+        out[r] = encode_e4m3(V[r] / s) * s
+    return out
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """float64 -> nearest fp32 -> nearest bf16 (ties to even), as float64."""
+    f = np.asarray(v, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return u.view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
 # Expert FFN (SwiGLU), shared expert, combine
 # --------------------------------------------------------------------------
 
@@ -204,13 +263,21 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
-def swiglu_ffn(X: np.ndarray, W13: np.ndarray, W2: np.ndarray) -> np.ndarray:
+def swiglu_ffn(X: np.ndarray, W13: np.ndarray, W2: np.ndarray, act: Optional[str] = None) -> np.ndarray:
     """O = (silu(X Wg^T) * (X Wu^T)) W2^T with W13 = [Wg; Wu] ([2f, d]) and
-    W2 [d, f]."""
+    W2 [d, f].  act = "e4m3": the rows of X, and of H after rounding to bf16,
+    go through quantize_act_rows first."""
     f = W2.shape[1]
+    if act == "e4m3":
+        X = quantize_act_rows(X)
+    elif act is not None:
+        raise ValueError(act)
     G = X @ W13[:f].T
     U = X @ W13[f:].T
-    return (silu(G) * U) @ W2.T
+    H = silu(G) * U
+    if act == "e4m3":
+        H = quantize_act_rows(round_bf16(H))
+    return H @ W2.T
 
 
 def expert_weights(inp, e: int):
@@ -238,7 +305,7 @@ def x_values(inp) -> np.ndarray:
     return np.asarray(inp.x, dtype=np.float64)
 
 
-def layer_forward(inp, want_intermediates: bool = True) -> Dict[str, np.ndarray]:
+def layer_forward(inp, want_intermediates: bool = True, act: Optional[str] = None) -> Dict[str, np.ndarray]:
     """Full layer on all T tokens.
 
     Returns y [T,d] = shared(x) + sum_j w[t,j] * FFN_{ids[t,j]}(x[t]), with the
@@ -260,9 +327,9 @@ def layer_forward(inp, want_intermediates: bool = True) -> Dict[str, np.ndarray]
         pairs = sorted_pair[a:b]
         tok = pairs // cfg.k
         W13, W2 = expert_weights(inp, e)
-        out_perm[a:b] = wflat[pairs][:, None] * swiglu_ffn(x[tok], W13, W2)
+        out_perm[a:b] = wflat[pairs][:, None] * swiglu_ffn(x[tok], W13, W2, act)
     S13, S2 = shared_weights(inp)
-    shared = swiglu_ffn(x, S13, S2)
+    shared = swiglu_ffn(x, S13, S2, act)
     y = shared.copy()
     for j in range(cfg.k):
         y += out_perm[row_of.reshape(cfg.T, cfg.k)[:, j]]
@@ -273,7 +340,8 @@ def layer_forward(inp, want_intermediates: bool = True) -> Dict[str, np.ndarray]
     return res
 
 
-def layer_forward_tokens(inp, tokens: Iterable[int], ids_override: Optional[np.ndarray] = None):
+def layer_forward_tokens(inp, tokens: Iterable[int], ids_override: Optional[np.ndarray] = None,
+                         act: Optional[str] = None):
     """y for a subset of tokens only (sampled checks at full size).
 
     Routing is computed for the listed tokens; each needed expert is
@@ -288,12 +356,12 @@ def layer_forward_tokens(inp, tokens: Iterable[int], ids_override: Optional[np.n
     ids = topk_ids(L, cfg.k) if ids_override is None else np.asarray(ids_override, np.int32)
     w = gates(L, ids)
     S13, S2 = shared_weights(inp)
-    y = swiglu_ffn(x, S13, S2)
+    y = swiglu_ffn(x, S13, S2, act)
     contrib = np.zeros((len(tokens), cfg.k, cfg.d), dtype=np.float64)
     for e in np.unique(ids):
         rows, slots = np.nonzero(ids == e)
         W13, W2 = expert_weights(inp, int(e))
-        contrib[rows, slots] = w[rows, slots][:, None] * swiglu_ffn(x[rows], W13, W2)
+        contrib[rows, slots] = w[rows, slots][:, None] * swiglu_ffn(x[rows], W13, W2, act)
     for j in range(cfg.k):
         y += contrib[:, j]
     return dict(y=y, logits=L, ids=ids, w=w)

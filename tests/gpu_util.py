@@ -70,19 +70,20 @@ def check_routing(inp, ids_gpu, w_gpu, offs_gpu):
 PARITY_LOG = []
 
 
-def check_output(inp, y_gpu, ids_gpu, tokens=None, max_abs_rms=MAX_ABS_RMS, ulp_rel=0.0):
+def check_output(inp, y_gpu, ids_gpu, tokens=None, max_abs_rms=MAX_ABS_RMS, ulp_rel=0.0, act=None):
     """rel-L2 <= REL_L2 and, element by element, |err| <= max_abs_rms * rms(y_ref)
     + ulp_rel * |y_ref| (ulp_rel = 0 except for a bf16 output, where one
-    rounding of the output itself is allowed on top)."""
+    rounding of the output itself is allowed on top).  act = "e4m3" compares
+    against the oracle's restatement of the 8-bit-activation mode."""
     if tokens is None:
         tokens = np.arange(inp.cfg.T)
-    ref = oracle.layer_forward_tokens(inp, tokens, ids_override=ids_gpu[tokens])["y"]
+    ref = oracle.layer_forward_tokens(inp, tokens, ids_override=ids_gpu[tokens], act=act)["y"]
     got = y_gpu[tokens].astype(np.float64)
     err = got - ref
     rel = np.linalg.norm(err) / np.linalg.norm(ref)
     rms = np.sqrt(np.mean(ref ** 2))
     mx = np.max(np.abs(err)) / rms
-    PARITY_LOG.append((inp.cfg.name, float(rel), float(mx)))
+    PARITY_LOG.append((inp.cfg.name + ("+act_e4m3" if act else ""), float(rel), float(mx)))
     bound = max_abs_rms * rms + ulp_rel * np.abs(ref)
     assert rel <= REL_L2 and np.all(np.abs(err) <= bound), f"rel_l2={rel:.3e} max_abs/rms={mx:.3e}"
     return rel, mx

@@ -54,7 +54,11 @@ def cfg(**kw):
     dict(T=-1), dict(d_model=100), dict(d_model=0), dict(d_model=32768), dict(n_experts=0),
     dict(n_experts=300), dict(top_k=0), dict(top_k=17), dict(n_experts=4, top_k=5), dict(d_ff=100),
     dict(d_ff_shared=0), dict(x_dtype=abi.MOE_E4M3), dict(w_dtype=abi.MOE_BF16), dict(y_dtype=abi.MOE_NVFP4),
-    dict(flags=0x80), dict(flags=0x8),
+    dict(flags=0x80), dict(flags=0x10),
+    # 8-bit activations only on the FP8 tensor-core path
+    dict(flags=abi.MOE_FLAG_ACT_E4M3, w_dtype=abi.MOE_NVFP4), dict(flags=abi.MOE_FLAG_ACT_E4M3, w_dtype=abi.MOE_F32),
+    dict(flags=abi.MOE_FLAG_ACT_E4M3, x_dtype=abi.MOE_F32), dict(flags=abi.MOE_FLAG_ACT_E4M3 | abi.MOE_FLAG_SIMT_FFN),
+    dict(flags=abi.MOE_FLAG_ACT_E4M3, d_ff=192),
 ])
 def test_invalid_config_rejected(lib, bad):
     c = cfg(**bad)
@@ -136,6 +140,10 @@ def test_no_cuda_device_reports_error(lib):
     c = cfg()
     fake = ctypes.c_void_p(0x10000)
     assert lib.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, None, 0, None) in (4, 7)
+
+
+def test_act_e4m3_flag_is_accepted(lib):
+    assert lib.moe_workspace_bytes(ctypes.byref(cfg(flags=abi.MOE_FLAG_ACT_E4M3))) > 0
 
 
 def test_test_hook_flag_is_accepted(lib):

@@ -244,6 +244,30 @@ def test_nonfinite_input_is_reported(T):
     assert abi.moe_get_device_status() == 0     # cleared
 
 
+# Opt-in 8-bit activations (MOE_FLAG_ACT_E4M3): parity against the oracle's
+# restatement of that rounding; the exact-activation oracle is a few percent
+# away, which is what the mode trades for half the MMA work.
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_act_e4m3_matches_its_oracle(name):
+    inp = workload(name)
+    _, _, y, ids, w, offs = run_layer(inp, abi.MOE_FLAG_ACT_E4M3)
+    check_routing(inp, ids, w, offs)
+    tokens = np.arange(inp.cfg.T) if inp.cfg.T <= 64 else sample_tokens(inp.cfg.T, 48)
+    check_output(inp, y, ids, tokens, act="e4m3")
+    exact = oracle.layer_forward_tokens(inp, tokens, ids_override=ids[tokens])["y"]
+    rel = np.linalg.norm(y[tokens] - exact) / np.linalg.norm(exact)
+    assert 5e-3 < rel < 0.15, rel
+
+
+@pytest.mark.parametrize("shape", [dict(T=64, d=256, E=16, k=2, f=128, fs=256),
+                                   dict(T=301, d=384, E=16, k=4, f=256, fs=384)], ids=["T64", "T301"])
+def test_act_e4m3_tiles(shape):
+    inp = moe_synth.make_custom(x_dtype="bf16", w_dtype="e4m3", seed=shape["T"] + 1, **shape)
+    _, _, y, ids, w, offs = run_layer(inp, abi.MOE_FLAG_ACT_E4M3)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids, act="e4m3")
+
+
 # Shapes whose average rows per expert select each tensor-core token tile
 # (TN = 8, 16, 32, 64, 128) with ragged last tiles, f != f_s, and a d that is
 # not a power of two.

@@ -360,3 +360,65 @@ def test_out_perm_rows_are_gate_weighted_expert_outputs():
         W13, W2 = oracle.expert_weights(inp, e)
         assert np.allclose(res["out_perm"][r], res["w"][t, j] * _torch_swiglu(x[t:t + 1], W13, W2)[0],
                            rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- 8-bit activations
+# (the restatement the library's opt-in MOE_FLAG_ACT_E4M3 mode is checked against)
+
+def test_encode_e4m3_matches_torch_cast():
+    rng = np.random.default_rng(21)
+    v = np.clip(rng.standard_normal(4000) * 60, -448, 448).astype(np.float32).astype(np.float64)
+    pos = oracle.moe_oracle._E4M3_POS
+    mids = (pos[:-1] + pos[1:]) / 2                      # exact ties between neighbouring codes
+    vals = np.concatenate([v, mids, -mids, pos, -pos])
+    ref = torch.tensor(vals, dtype=torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.encode_e4m3(vals), ref)
+
+
+def test_act_scale_is_the_smallest_power_of_two():
+    rng = np.random.default_rng(22)
+    amaxes = np.concatenate([np.exp(rng.uniform(-60, 60, 400)), [448.0, 449.0, 224.0, 224.5, 3.5, 1.0, 1e-38]])
+    for amax in amaxes:
+        s = oracle.act_scale(float(amax))
+        m, _ = math.frexp(s)
+        assert m == 0.5                                   # a power of two
+        assert amax <= 448.0 * s
+        assert amax > 224.0 * s or s == 2.0 ** -126       # and no smaller one would do
+    assert oracle.act_scale(448.0) == 1.0 and oracle.act_scale(448.5) == 2.0
+    assert oracle.act_scale(0.0) == 1.0 and oracle.act_scale(float("nan")) == 1.0
+
+
+def test_quantize_act_rows_error_bounds_and_idempotence():
+    rng = np.random.default_rng(23)
+    X = rng.standard_normal((6, 300)) * np.exp(rng.uniform(-6, 6, (6, 1)))
+    Q = oracle.quantize_act_rows(X)
+    for r in range(X.shape[0]):
+        s = oracle.act_scale(float(np.abs(X[r]).max()))
+        normal = np.abs(X[r]) >= 2.0 ** -6 * s
+        err = np.abs(Q[r] - X[r])
+        assert np.all(err[normal] <= 2.0 ** -4 * np.abs(X[r][normal]))   # half an ulp of 3 mantissa bits
+        assert np.all(err[~normal] <= 2.0 ** -10 * s)                    # half the subnormal step
+        assert np.abs(Q[r]).max() <= 448.0 * s
+    assert np.array_equal(oracle.quantize_act_rows(Q), Q)
+
+
+def test_round_bf16_matches_torch():
+    rng = np.random.default_rng(24)
+    v = (rng.standard_normal(3000) * np.exp(rng.uniform(-20, 20, 3000))).astype(np.float32)
+    ref = torch.tensor(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_bf16(v.astype(np.float64)), ref)
+
+
+def test_act_e4m3_ffn_is_near_but_not_equal():
+    # the lossy mode stays within a few E4M3 roundings of the exact FFN
+    rng = np.random.default_rng(25)
+    X = rng.standard_normal((12, 64))
+    W13 = rng.standard_normal((2 * 32, 64)) / 8
+    W2 = rng.standard_normal((64, 32)) / 6
+    exact = oracle.swiglu_ffn(X, W13, W2)
+    lossy = oracle.swiglu_ffn(X, W13, W2, act="e4m3")
+    rel = np.linalg.norm(lossy - exact) / np.linalg.norm(exact)
+    assert 1e-3 < rel < 0.15
+    # inputs already on the scaled E4M3 grid pass the first rounding unchanged
+    Xq = oracle.quantize_act_rows(X)
+    assert np.array_equal(oracle.quantize_act_rows(Xq), Xq)

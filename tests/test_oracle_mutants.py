@@ -35,12 +35,12 @@ def _silu_wrong_sign(z):
     return z / (1.0 + np.exp(z))
 
 
-def _swiglu_swapped(X, W13, W2):
+def _swiglu_swapped(X, W13, W2, act=None):
     f = W2.shape[1]
     return (om.silu(X @ W13[f:].T) * (X @ W13[:f].T)) @ W2.T
 
 
-def _swiglu_w2_transposed(X, W13, W2):
+def _swiglu_w2_transposed(X, W13, W2, act=None):
     f = W2.shape[1]
     return (om.silu(X @ W13[:f].T) * (X @ W13[f:].T)) @ W2
 
@@ -74,9 +74,23 @@ def _e2m1_nibbles_swapped(packed):
     return out
 
 
-def _swiglu_no_silu(X, W13, W2):
+def _swiglu_no_silu(X, W13, W2, act=None):
     f = W2.shape[1]
     return ((X @ W13[:f].T) * (X @ W13[f:].T)) @ W2.T
+
+
+def _encode_truncating(v):
+    v = np.asarray(v, dtype=np.float64)
+    pos = om._E4M3_POS
+    i = np.clip(np.searchsorted(pos, np.abs(v), side="right") - 1, 0, 126)
+    return np.sign(v) * pos[i]
+
+
+def _act_scale_doubled(amax):
+    return 2.0 * _orig_act_scale(amax)
+
+
+_orig_act_scale = om.act_scale
 
 
 MUTANTS = [
@@ -90,6 +104,8 @@ MUTANTS = [
     ("permute", _permute_by_token, pins.test_permute_bruteforce_and_invariants, (7, 8, 3)),
     ("router_logits", _logits_ignore_bias, pins.test_router_logits_bias_and_linearity, ()),
     ("decode_e2m1_packed", _e2m1_nibbles_swapped, pins.test_e2m1_packing_nibble_order, ()),
+    ("encode_e4m3", _encode_truncating, pins.test_encode_e4m3_matches_torch_cast, ()),
+    ("act_scale", _act_scale_doubled, pins.test_act_scale_is_the_smallest_power_of_two, ()),
 ]
 
 

@@ -20,6 +20,7 @@ MOE_F32, MOE_BF16, MOE_E4M3, MOE_NVFP4 = 0, 1, 2, 3
 MOE_FLAG_SIMT_FFN = 0x1
 MOE_FLAG_SIMT_ROUTER = 0x2
 MOE_FLAG_BF16_EXPERT_OUT = 0x4
+MOE_FLAG_ACT_E4M3 = 0x8
 MOE_FLAG_INJECT_TIMEOUT = 0x100
 MOE_NOALLOC_MAX_PAIRS = 65536
 

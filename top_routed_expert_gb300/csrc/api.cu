@@ -102,7 +102,13 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_E4M3 && c->w_dtype != MOE_NVFP4) return MOE_ERR_INVALID_ARG;
   if (c->y_dtype != MOE_F32 && c->y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(c->T) * c->top_k > (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER | MOE_FLAG_BF16_EXPERT_OUT | MOE_FLAG_INJECT_TIMEOUT)) != 0)
+  if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER | MOE_FLAG_BF16_EXPERT_OUT | MOE_FLAG_ACT_E4M3 |
+                    MOE_FLAG_INJECT_TIMEOUT)) != 0)
+    return MOE_ERR_INVALID_ARG;
+  // 8-bit activations exist only on the tensor-core FP8 path
+  if ((c->flags & MOE_FLAG_ACT_E4M3) &&
+      (c->w_dtype != MOE_E4M3 || c->x_dtype != MOE_BF16 || (c->flags & MOE_FLAG_SIMT_FFN) || c->d_ff % 128 != 0 ||
+       c->d_ff_shared % 128 != 0))
     return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
@@ -262,6 +268,7 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float*
   if (use_tc(*cfg))
     return cuda_status(launch_ffn_tc(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
                                      ws, di.status, di.num_sms, s));
+  if (cfg->flags & MOE_FLAG_ACT_E4M3) return MOE_ERR_UNSUPPORTED;   // no tensor-map encoder in this driver
   if (use_fp4(*cfg))
     return cuda_status(launch_ffn_fp4(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
                                       ws, di.status, di.num_sms, s));

@@ -15,6 +15,9 @@
 //    the product equals the bf16-activation product; hi and lo are adjacent
 //    N columns and the epilogue adds them.  Per-channel weight scales and the
 //    row scale are applied in the epilogue.
+//  * MOE_FLAG_ACT_E4M3 (opt-in, lossy): one E4M3 term per activation with
+//    the same per-row power-of-two scale, so N is the token count and the MMAs
+//    issue the layer's FLOPs once (TERMS = 1 below).
 //  * gemm1 (gate+up, two accumulators) -> silu(g)*u -> H (bf16);
 //    H is re-split into two E4M3 terms per row; gemm2 (down) applies the gate
 //    weight and writes out_perm (routed) / shared_out (shared expert).
@@ -69,7 +72,7 @@ struct TcArgs {
   void* shared_out;            // gemm2 out: [T][d]
   bool out_bf16;
   int T, k, E, P, d, f, fs, fmax;
-  int TN;                      // token rows per tile; MMA N = 2*TN
+  int TN;                      // token rows per tile; MMA N = TERMS*TN
   int stages, acc_bufs, tmem_cols;
   uint64_t wait_ns;            // limit of every bounded wait
   int inject_drop;             // test hook: CTA 0 withholds its first "accumulator ready"
@@ -85,18 +88,20 @@ struct __align__(16) TcCtrl {
   uint64_t ep_sync;            // the eight epilogue warps meet here once per tile
   uint32_t tmem_base;
   int abort;
-  float coef[2][kBM];          // per-row epilogue coefficient, double-buffered by tile parity
+  float coef[2][2 * kBM];      // per-row epilogue coefficient (TN <= 256), double-buffered by tile parity
   GroupTable gt;
 };
 
-template <int MODE>
+// TERMS = activation terms per token row: 2 (exact split, default) or 1
+// (MOE_FLAG_ACT_E4M3).  The B operand holds TERMS adjacent rows per token.
+template <int MODE, int TERMS>
 __global__ void __launch_bounds__(kTcThreads, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAS,
               const __grid_constant__ CUtensorMap mapB, TcArgs a) {
   constexpr int NA = (MODE == 1) ? 2 : 1;   // weight tiles per stage (gate + up, or down)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int N = 2 * a.TN;
+  const int N = TERMS * a.TN;
   const uint32_t b_bytes = static_cast<uint32_t>(N) * kBK;
   const uint32_t stage_bytes = NA * kABytes + ((b_bytes + 1023u) & ~1023u);
   TcCtrl* c = reinterpret_cast<TcCtrl*>(smem + a.stages * stage_bytes);
@@ -159,7 +164,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           arow0 = (shr ? 0 : t.g * a.d) + t.wt * kBM;
           K = shr ? a.fs : a.f;
         }
-        const int brow = 2 * t.row0;
+        const int brow = TERMS * t.row0;
         for (int kb = 0; kb < K / kBK; ++kb) {
           if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, a.wait_ns)) break;
           const uint32_t full = smem_u32(&c->full[st]);
@@ -248,7 +253,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       // Per-row coefficients of this tile, loaded while the MMAs run: the
       // row's activation scale, times the gate weight of its (token, slot)
       // pair in the down projection.
-      if (et < kBM) {
+      if (et < a.TN) {
         float cf = 0.f;
         if (et < t.nrows) {
           const int row = t.row0 + et;
@@ -280,20 +285,23 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const float sg = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + col];
         const float su = shr ? a.as_scale[width + col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + a.f + col];
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
-        // chunks of 32 columns = 16 token rows; N is a multiple of 16 and a
-        // 32-wide load past N stays inside the allocation
+        // chunks of 32 columns = 32 / TERMS token rows; N is a multiple of
+        // 16 and a 32-wide load past N stays inside the allocation
+        constexpr int TPC = 32 / TERMS;
         for (int c0 = 32 * half; c0 < N; c0 += 64) {
-          float gv[32], uv[32], cf[16];
+          float gv[32], uv[32], cf[TPC];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) cf[jj] = coef[c0 / 2 + jj];
+          for (int jj = 0; jj < TPC; ++jj) cf[jj] = coef[c0 / TERMS + jj];
           tmem_ld32x2(cb + c0, cb + N + c0, gv, uv);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = c0 / 2 + jj;
+          for (int jj = 0; jj < TPC; ++jj) {
+            const int j = c0 / TERMS + jj;
             if (j < t.nrows) {
               const int row = t.row0 + j;
-              const float g = (gv[2 * jj] + gv[2 * jj + 1] * 0.0625f) * cf[jj] * sg;
-              const float u = (uv[2 * jj] + uv[2 * jj + 1] * 0.0625f) * cf[jj] * su;
+              const float gd = TERMS == 2 ? gv[2 * jj] + gv[2 * jj + 1] * 0.0625f : gv[jj];
+              const float ud = TERMS == 2 ? uv[2 * jj] + uv[2 * jj + 1] * 0.0625f : uv[jj];
+              const float g = gd * cf[jj] * sg;
+              const float u = ud * cf[jj] * su;
               a.h[static_cast<size_t>(row) * a.fmax + col] = __float2bfloat16_rn(silu(g) * u);
             }
           }
@@ -303,20 +311,30 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
         void* outp = shr ? a.shared_out : a.out_perm;
         const size_t out0 = static_cast<size_t>(shr ? t.row0 - a.P : t.row0) * a.d + col;
-        // chunks of 64 columns = 32 token rows
+        // chunks of 64 columns = 64 / TERMS token rows
+        constexpr int TPC = 64 / TERMS;
         for (int c0 = 64 * half; c0 < N; c0 += 128) {
-          float d0[32], d1[32], cf[32];
+          float d0[32], d1[32];
+          float cf[TERMS == 2 ? TPC : 1];   // two terms: this chunk's coefficients in registers
+          if (TERMS == 2) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) cf[jj] = coef[c0 / 2 + jj];
+            for (int jj = 0; jj < TPC; ++jj) cf[jj] = coef[c0 / TERMS + jj];
+          }
           tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int j = c0 / 2 + jj;
+          for (int jj = 0; jj < TPC; ++jj) {
+            const int j = c0 / TERMS + jj;
             if (j < t.nrows) {
-              const float* dv = jj < 16 ? d0 : d1;
-              const int q = 2 * (jj & 15);
-              store_out(outp, out0 + static_cast<size_t>(j) * a.d, (dv[q] + dv[q + 1] * 0.0625f) * cf[jj] * sw,
-                        a.out_bf16);
+              float dsum;
+              if (TERMS == 2) {
+                const float* dv = jj < 16 ? d0 : d1;
+                const int q = 2 * (jj & 15);
+                dsum = dv[q] + dv[q + 1] * 0.0625f;
+              } else {
+                dsum = jj < 32 ? d0[jj] : d1[jj - 32];
+              }
+              const float cfj = TERMS == 2 ? cf[TERMS == 2 ? jj : 0] : coef[j];
+              store_out(outp, out0 + static_cast<size_t>(j) * a.d, dsum * cfj * sw, a.out_bf16);
             }
           }
         }
@@ -338,8 +356,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------
-// Row quantiser: v = s * (hi + lo/16), s = 2^ceil(log2(amax/448)), hi and lo
-// E4M3 (round to nearest even, saturating).  One warp per row of the
+// Row quantiser: v = s * (hi + lo/16), s = the smallest power of two with
+// amax <= 448 s (1 for an all-zero row), hi and lo E4M3 (round to nearest
+// even, saturating).  With two_terms false only hi is written: the single-
+// term 8-bit activation of MOE_FLAG_ACT_E4M3.  One warp per row of the
 // (P+T)-row activation space.  GATHER_X: row r < P takes x[sorted_pair[r]/k],
 // row P+t takes x[t] (width d); otherwise row r of H (width f for routed
 // rows, f_s for shared rows).  Output q[2r] = hi codes, q[2r+1] = lo codes.
@@ -347,7 +367,7 @@ template <bool GATHER_X, bool IN_REGS>
 __global__ void __launch_bounds__(256)
 quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                    int width_r, int width_s, int src_stride, uint8_t* __restrict__ q, int q_stride,
-                   float* __restrict__ scale, unsigned* status) {
+                   float* __restrict__ scale, bool two_terms, unsigned* status) {
   pdl_enter();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -367,7 +387,7 @@ quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__
       if (lane == 0) set_status(status, MOE_ERR_DEVICE_BOUNDS);
       for (int c = lane * 8; c < width; c += 256) {
         *reinterpret_cast<uint2*>(qh + c) = make_uint2(0, 0);
-        *reinterpret_cast<uint2*>(ql + c) = make_uint2(0, 0);
+        if (two_terms) *reinterpret_cast<uint2*>(ql + c) = make_uint2(0, 0);
       }
       if (lane == 0) scale[row] = 1.f;
       return;
@@ -411,12 +431,15 @@ quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  // amax = m 2^e with m in [0.5, 1): 448 * 2^(e-9) = 0.875 * 2^e is the
+  // smallest candidate (448 * 2^(e-10) < 2^(e-1) <= amax); both comparisons
+  // are exact in fp32
   float sc = 1.f;
   if (amax > 0.f && isfinite(amax)) {
     int e;
-    const float m = frexpf(amax * (1.0f / 448.0f), &e);   // amax/448 = m * 2^e, m in [0.5, 1)
-    sc = ldexpf(1.0f, m == 0.5f ? e - 1 : e);
-    if (amax / sc > 448.0f) sc *= 2.0f;
+    frexpf(amax, &e);
+    sc = ldexpf(1.0f, max(e - 9, -126));
+    if (amax > 448.0f * sc) sc *= 2.0f;
   }
   const float inv = 1.0f / sc;   // exact: sc is a power of two
   auto emit = [&](int c, const uint4& v) {
@@ -434,7 +457,7 @@ quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__
       lo[i >> 1] |= static_cast<uint32_t>(l2) << (16 * (i & 1));
     }
     *reinterpret_cast<uint2*>(qh + c) = make_uint2(hi[0], hi[1]);
-    *reinterpret_cast<uint2*>(ql + c) = make_uint2(lo[0], lo[1]);
+    if (two_terms) *reinterpret_cast<uint2*>(ql + c) = make_uint2(lo[0], lo[1]);
   };
   if (in_regs) {
 #pragma unroll
@@ -470,13 +493,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D byte matrix [rows][cols] (row pitch = cols bytes), box 128 bytes x box_rows,
-// 128-byte swizzle; rows past the end read as zero.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D byte matrix [rows][cols] (row pitch = pitch bytes, default cols), box 128
+// bytes x box_rows, 128-byte swizzle; rows past the end read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              uint64_t pitch = 0) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols};
+  cuuint64_t strides[1] = {pitch ? pitch : cols};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -506,11 +530,11 @@ TcPlan plan(const moe_config_t& c) {
   return p;
 }
 
-template <int MODE>
+template <int MODE, int TERMS>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUtensorMap& mB, TcArgs a,
                         int wtiles_max, int num_sms, cudaStream_t stream) {
   constexpr int NA = (MODE == 1) ? 2 : 1;
-  const int N = 2 * a.TN;
+  const int N = TERMS * a.TN;
   const int stage_bytes = NA * kABytes + align_up(static_cast<size_t>(N) * kBK, 1024);
   a.stages = std::min(kMaxStages, kSmemBudget / stage_bytes);
   const int per_acc = NA * N;
@@ -526,13 +550,14 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUt
   a.tmem_cols = cols;
   size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + sizeof(TcCtrl);
   smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
-  cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_tc_kernel<MODE>), static_cast<int>(smem));
+  cudaError_t err =
+      ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_tc_kernel<MODE, TERMS>), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const long long tiles_ub =
       static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
   count_launches(1);
-  return launch_pdl(ffn_tc_kernel<MODE>, grid, kTcThreads, smem, stream, mA, mAS, mB, a);
+  return launch_pdl(ffn_tc_kernel<MODE, TERMS>, grid, kTcThreads, smem, stream, mA, mAS, mB, a);
 }
 
 }  // namespace
@@ -552,6 +577,15 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   const int P = T * k, R = P + T;
   const int fmax = std::max(f, fs);
   const TcPlan pl = plan(c);
+  // activation terms per row: 2 (exact), or 1 with MOE_FLAG_ACT_E4M3 (the
+  // MMA's N is then the token count, at least 16)
+  const bool one_term = (c.flags & MOE_FLAG_ACT_E4M3) != 0;
+  const int tn1 = one_term ? std::max(16, std::min(pl.TN, 128)) : std::min(pl.TN, MOE_TC_TN1_CAP);
+  // one term, down GEMM: 256-token tiles once groups are that large (N = 256
+  // halves the operand bytes per MAC of a 128 x 128 tile; K = f is short, so
+  // the feed, not the MMA, bounds the smaller tile)
+  const int tn2 = one_term ? (static_cast<double>(P) / E > 96 ? 256 : std::max(16, std::min(pl.TN, 128)))
+                           : std::min(pl.TN, MOE_TC_TN2_CAP);
   char* base = static_cast<char*>(ws);
   uint8_t* xq = reinterpret_cast<uint8_t*>(base + pl.xq);
   float* sx = reinterpret_cast<float*>(base + pl.sx);
@@ -566,7 +600,7 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   count_launches(1);
   cudaError_t err = launch_pdl(regs ? quant2_rows_kernel<true, true> : quant2_rows_kernel<true, false>, qblocks, 256, 0,
                                stream, static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d, d, d, xq, d, sx,
-                               status);
+                               !one_term, status);
   if (err != cudaSuccess) return err;
 
   CUtensorMap mA, mAS, mB;
@@ -580,34 +614,39 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   a.wait_ns = inject ? 20000000ull : kWaitLimitNs;
   a.inject_drop = inject ? 1 : 0;
 
-  // gemm1: gate/up
+  // gemm1: gate/up (B: both term rows of each activation row, or the hi rows only)
+  const bool mb_ok = one_term ? make_map(&mB, xq, static_cast<uint64_t>(R), d, tn1, 2 * static_cast<uint64_t>(d))
+                              : make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * tn1);
   if (!make_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, kBM) ||
-      !make_map(&mAS, w->s13, static_cast<uint64_t>(2) * fs, d, kBM) ||
-      !make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * std::min(pl.TN, MOE_TC_TN1_CAP)))
+      !make_map(&mAS, w->s13, static_cast<uint64_t>(2) * fs, d, kBM) || !mb_ok)
     return cudaErrorInvalidValue;
   a.a_scale = static_cast<const float*>(w->w13_scale);
   a.as_scale = static_cast<const float*>(w->s13_scale);
   a.b_scale = sx;
-  a.TN = std::min(pl.TN, MOE_TC_TN1_CAP);   // 2 x (gate, up) x 2*TN columns fit TMEM twice over at 64
-  err = launch_gemm<1>(mA, mAS, mB, a, std::max(f, fs) / kBM, num_sms, stream);
+  a.TN = tn1;   // two buffers of (gate, up) x TERMS*TN columns fit TMEM at TERMS*TN <= 128
+  err = one_term ? launch_gemm<1, 1>(mA, mAS, mB, a, std::max(f, fs) / kBM, num_sms, stream)
+                 : launch_gemm<1, 2>(mA, mAS, mB, a, std::max(f, fs) / kBM, num_sms, stream);
   if (err != cudaSuccess) return err;
 
   count_launches(1);
   err = launch_pdl(regs ? quant2_rows_kernel<false, true> : quant2_rows_kernel<false, false>, qblocks, 256, 0, stream,
                    reinterpret_cast<const uint16_t*>(h), static_cast<const int32_t*>(nullptr), P, T, k, f, fs, fmax,
-                   hq, fmax, sh, status);
+                   hq, fmax, sh, !one_term, status);
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs
+  const bool mb2_ok = one_term
+                          ? make_map(&mB, hq, static_cast<uint64_t>(R), fmax, tn2, 2 * static_cast<uint64_t>(fmax))
+                          : make_map(&mB, hq, static_cast<uint64_t>(2) * R, fmax, 2 * tn2);
   if (!make_map(&mA, w->w2, static_cast<uint64_t>(E) * d, f, kBM) ||
-      !make_map(&mAS, w->s2, static_cast<uint64_t>(d), fs, kBM) ||
-      !make_map(&mB, hq, static_cast<uint64_t>(2) * R, fmax, 2 * std::min(pl.TN, MOE_TC_TN2_CAP)))
+      !make_map(&mAS, w->s2, static_cast<uint64_t>(d), fs, kBM) || !mb2_ok)
     return cudaErrorInvalidValue;
   a.a_scale = static_cast<const float*>(w->w2_scale);
   a.as_scale = static_cast<const float*>(w->s2_scale);
   a.b_scale = sh;
-  a.TN = std::min(pl.TN, MOE_TC_TN2_CAP);
-  return launch_gemm<2>(mA, mAS, mB, a, d / kBM, num_sms, stream);
+  a.TN = tn2;
+  return one_term ? launch_gemm<2, 1>(mA, mAS, mB, a, d / kBM, num_sms, stream)
+                  : launch_gemm<2, 2>(mA, mAS, mB, a, d / kBM, num_sms, stream);
 }
 
 }  // namespace moe
