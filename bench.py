@@ -122,13 +122,12 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.1)
         return self
 
     def __exit__(self, *a):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.25)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -156,6 +155,17 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def keep_busy(step, seconds, torch, dev):
+    """Untimed passes for about `seconds` (in groups of 8, synchronised), so
+    that the clock samples around a short timed region see the GPU under the
+    same load and nvidia-smi's start-up falls outside the timed region."""
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        for _ in range(8):
+            step()
+        torch.cuda.synchronize(dev)
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -301,14 +311,16 @@ def measure(layer, x, cfg, steps, warmup, world, dev, gpu_index, abi, torch, clo
     counts = np.diff(offs.cpu().numpy())
     alg = algorithmic(cfg, counts)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
-    launches0 = abi.moe_launch_count()
-    barrier()
     clk = ClockSampler(gpu_index if clocks else None)
     with clk:
+        keep_busy(step, 0.4 if clocks else 0.0, torch, dev)
+        barrier()
+        launches0 = abi.moe_launch_count()
         for i in range(steps):
             step(evs[i])
         barrier()
-    launches = abi.moe_launch_count() - launches0
+        launches = abi.moe_launch_count() - launches0   # this library's kernels in the timed steps
+        keep_busy(step, 0.3 if clocks else 0.0, torch, dev)
     st = abi.moe_get_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {abi.STATUS.get(st, st)}")
@@ -338,6 +350,11 @@ def time_graph(layer, x, steps, warmup, world, dev, torch, gpu_index=None):
     torch.cuda.synchronize(dev)
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_index) as clk:
+        keep_busy(graph.replay, 0.4, torch, dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
         g0.record(stream)
         for _ in range(steps):
             graph.replay()
@@ -346,6 +363,7 @@ def time_graph(layer, x, steps, warmup, world, dev, torch, gpu_index=None):
             import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize(dev)
+        keep_busy(graph.replay, 0.3, torch, dev)
     ms = g0.elapsed_time(g1) / steps
     if world > 1:
         import torch.distributed as dist
@@ -520,9 +538,11 @@ def run_ours(args, world, rank, local):
                                    "exact (bf16, or two E4M3 terms per row on the FP8 tensor cores)"),
                    "expert_out": "bf16" if args.bf16_expert_out else "fp32",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: expert weights %.2f GB per pass" % (m["alg"]["ffn_bytes"] / 1e9)},
+                   "l2": "inputs larger than L2 (no flush needed): the expert stage moves %.2f GB per pass, "
+                         "the expert weights alone over 1.5 GB" % (m["alg"]["ffn_bytes"] / 1e9)},
         "timing": "each step replays the layer captured as one CUDA graph; stream_launch times the same "
-                  "step launched call by call, with CUDA events between the stages",
+                  "step launched call by call, with CUDA events between the stages; clocks are sampled while "
+                  "the layer runs (the timed steps plus ~0.7 s of untimed passes around them)",
         "stream_launch": {"ms_per_step": m["ms_step"], "value": world * T / (m["ms_step"] / 1e3),
                           "stages_ms": m["stage_ms"], "clocks": m["clocks"]},
         "roofline": roof,
