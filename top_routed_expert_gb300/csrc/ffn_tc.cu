@@ -25,9 +25,10 @@
 //  * persistent CTAs walk a device-built tile list (group, weight tile,
 //    token tile) -- no host read-back of the expert counts.
 //  * warp roles: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
-//    warps 2-5 = epilogue.  Every mbarrier wait is bounded; on expiry the
-//    kernel records MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs,
-//    frees TMEM and returns.
+//    warps 2-9 = epilogue (two per TMEM sub-partition).
+//  * every mbarrier wait is bounded; on expiry the kernel records
+//    MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and
+//    returns.
 #include <cuda.h>
 
 #include "common.cuh"
