@@ -1,0 +1,62 @@
+"""Host-side checks of bench.py's bookkeeping (no GPU): the roofline bound it
+reports, the issued-MMA factor of each activation mode, and that a recorded
+ncu traffic figure is used only for the sources it was taken on."""
+import json
+import os
+
+import pytest
+
+import bench
+
+PEAKS = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+
+
+@pytest.fixture(autouse=True)
+def fixed_peaks(monkeypatch):
+    monkeypatch.setattr(bench, "load_peaks", lambda: (dict(PEAKS), "measured"))
+
+
+def alg(bytes_, flops):
+    return dict(active=128, ffn_bytes=bytes_, layer_bytes=bytes_, ffn_flops=flops, layer_flops=flops)
+
+
+def test_decode_is_hbm_bound():
+    roof, layer = bench.roofline(alg(1.6e9, 1.0e10), 0.32, 0.40, "decode")
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    assert roof["achieved"] == pytest.approx(1.6e9 / 0.32e-3 / 1e9)
+    assert roof["frac"] == pytest.approx(roof["achieved"] / 6000.0)
+    assert layer == pytest.approx((1.6e9 / 6000e9) / 0.40e-3)
+
+
+def test_prefill_reports_the_tensor_bound_and_issued_flops():
+    roof, _ = bench.roofline(alg(2.6e9, 1.44e12), 1.3, 1.6, "prefill", "e4m3")
+    assert roof["bound"] == "tensor" and roof["peak"] == pytest.approx(4000.0)     # FP8 = 2 x bf16
+    assert roof["achieved"] == pytest.approx(1.44e12 / 1.3e-3 / 1e12)
+    assert roof["issued"]["tflops"] == pytest.approx(2 * roof["achieved"])           # two E4M3 terms
+    one, _ = bench.roofline(alg(2.6e9, 1.44e12), 0.9, 1.1, "prefill", "e4m3", False, 1)
+    assert one["issued"]["tflops"] == pytest.approx(one["achieved"])                 # one term
+    fp4, _ = bench.roofline(alg(2.6e9, 3.7e12), 4.9, 5.2, "100b_prefill", "nvfp4")
+    assert fp4["peak"] == pytest.approx(8000.0)                                      # FP4 = 4 x bf16
+    assert fp4["issued"]["peak"] == pytest.approx(2000.0)                            # f16 MMAs
+
+
+def test_traffic_only_for_matching_sources(tmp_path, monkeypatch):
+    kernel = "moe_expert_ffn (grouped SwiGLU GEMMs + shared expert)"
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda: "abc")
+    rec = {"decode": {"kernel": kernel, "source_hash": "abc", "dram_bytes_per_launch": 123}}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    assert bench.recorded_traffic("decode", kernel) == 123
+    assert bench.recorded_traffic("prefill", kernel) is None
+    rec["decode"]["source_hash"] = "other"
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    assert bench.recorded_traffic("decode", kernel) is None
+
+
+def test_source_hash_covers_the_kernel_sources():
+    h = bench.source_hash()
+    assert len(h) == 16 and int(h, 16) >= 0
+    csrc = os.path.join(bench.ROOT, "top_routed_expert_gb300", "csrc")
+    assert any(fn.endswith(".cu") for fn in os.listdir(csrc))
