@@ -517,7 +517,7 @@ def run_ours(args, world, rank, local):
     roof, layer_frac = roofline(m["alg"], m["stage_ms"]["expert_ffn"], graph_ms, args.workload, cfg.w_dtype,
                                 args.simt, 1 if args.act_e4m3 else 2)
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:   # the oracle baseline: rank 0 of a single-GPU run only
         v, n, el = time_oracle(inp, args.cpu_budget)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
                "sample": f"{n} of the {T} tokens of this workload through the fp64 CPU oracle ({el:.1f} s)"}

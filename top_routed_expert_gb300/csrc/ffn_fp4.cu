@@ -568,7 +568,8 @@ scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict_
 #pragma unroll
     for (int i = 0; i < (IN_REGS ? kRegChunks : 1); ++i) absmax8(reg[i]);
   } else {
-    for (int c = lane * 8; c < width; c += 256) absmax8(*reinterpret_cast<const uint4*>(s + c));
+#pragma unroll 4
+    for (int c = lane * 8; c < width; c += 256) absmax8(*reinterpret_cast<const uint4*>(s + c));   // 4 loads in flight
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -596,6 +597,7 @@ scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict_
       if (c < width) emit(c, reg[i]);
     }
   } else {
+#pragma unroll 4
     for (int c = lane * 8; c < width; c += 256) emit(c, *reinterpret_cast<const uint4*>(s + c));
   }
   if (lane == 0) scale[row] = sc;

@@ -420,7 +420,8 @@ quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__
       }
     }
   } else {
-    for (int c = lane * 8; c < width; c += 256) {
+#pragma unroll 4
+    for (int c = lane * 8; c < width; c += 256) {   // four loads in flight per lane
       const uint4 v = *reinterpret_cast<const uint4*>(s + c);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -467,6 +468,7 @@ quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__
       if (c < width) emit(c, reg[i]);
     }
   } else {
+#pragma unroll 4
     for (int c = lane * 8; c < width; c += 256) emit(c, *reinterpret_cast<const uint4*>(s + c));
   }
   if (lane == 0) scale[row] = sc;
