@@ -9,6 +9,7 @@ reports MOE_ERR_CUDA / MOE_ERR_ARCH when called there).
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -47,7 +48,20 @@ def _stale(objs) -> bool:
 
 
 def build(verbose: bool = False, force: bool = False) -> str:
+    """Compile and link if anything changed.  Several processes may call this
+    at once (one per rank of a multi-GPU run): an exclusive lock on a file in
+    the build folder serialises them, and the later ones find the library
+    up to date."""
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(verbose, force)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool, force: bool) -> str:
     srcs = sources()
     objs = [os.path.join(BUILD, s[:-3] + ".o") for s in srcs]
     if not force and not _stale(objs):
