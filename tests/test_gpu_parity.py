@@ -63,6 +63,16 @@ def test_edge_shapes(T, E, k):
         assert np.all(w == 1.0)
 
 
+@pytest.mark.parametrize("w_dtype", ["e4m3", "nvfp4"])
+def test_largest_hidden_size(w_dtype):
+    # d_model = 16384, the largest the ABI accepts: the router's widest
+    # slices and the row quantisers' loop path (rows longer than 4096)
+    inp = moe_synth.make_custom(T=40, d=16384, E=8, k=2, f=128, fs=128, x_dtype="bf16", w_dtype=w_dtype, seed=16)
+    _, _, y, ids, w, offs = run_layer(inp)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids)
+
+
 def test_skew_has_empty_and_hot_experts():
     inp = workload("skew")
     _, _, _, ids, _, offs = run_layer(inp)
