@@ -23,8 +23,7 @@ What the layer computes (sources, by page and section):
   softmax over the expert logits followed by a top-k; section 3.3: the router
   emits int32 indices and fp32 weights per token.
 
-Readings where the pages are silent (each one is listed with its reason in the
-design notes of the repository):
+Readings where the pages are silent (the plainest reading in each case):
   softmax scoring; gates renormalised over the selected k; ties broken by the
   lowest expert index; one shared expert with weight 1; SwiGLU experts
   (silu(gate) * up, then down) with gate rows first in W13; an optional
