@@ -203,7 +203,7 @@ def permute(ids: np.ndarray, E: int):
 #   value      s * E4M3(v / s), E4M3 = nearest value, ties to the even code;
 #   H          rounded to fp32, then to bf16 (nearest even) before that.
 # The pages fix only the weight formats; this is the 8-bit-activation
-# reading of their FP8 compute, listed with the other readings.
+# reading of their FP8 compute.
 # --------------------------------------------------------------------------
 
 # finite non-negative E4M3 values, code 0 .. 126 (ascending with the code)
