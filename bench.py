@@ -171,18 +171,42 @@ def keep_busy(step, seconds, torch, dev):
 # ------------------------------------------------------------------ CPU oracle timing
 
 def time_oracle(inp, budget_s, chunk=2):
-    """Oracle tokens/s on a bounded sample: tokens in chunks until the budget."""
+    """Oracle tokens/s on a bounded sample: consecutive tokens in chunks
+    (wrapping around the batch) until the budget is spent, at least one chunk."""
     import oracle
     T = inp.cfg.T
-    done, t0 = 0, time.perf_counter()
-    while done < T:
-        n = min(chunk, T - done)
-        oracle.layer_forward_tokens(inp, range(done, done + n))
+    done, pos, t0 = 0, 0, time.perf_counter()
+    while True:
+        n = min(chunk, T - pos)
+        oracle.layer_forward_tokens(inp, range(pos, pos + n))
         done += n
+        pos = (pos + n) % T
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
     return done / el, done, el
+
+
+def oracle_one_thread(name, budget_s):
+    """The oracle on one host thread (BLAS and OpenMP pools limited to one
+    thread in a child process, set before numpy loads): tokens/s of `name`."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", name, "--cpu-budget", str(budget_s),
+           "--warmup", "3"]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=300)
+        line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1]
+        return json.loads(line)
+    except (subprocess.SubprocessError, IndexError, ValueError) as e:
+        return {"unavailable": f"{type(e).__name__}"}
+
+
+def oracle_sample_main(name, budget_s):
+    import moe_synth
+    inp = moe_synth.make_inputs(name)
+    v, n, el = time_oracle(inp, budget_s)
+    print(json.dumps({"value": v, "unit": "tokens/s", "threads": 1, "tokens": n, "seconds": el}), flush=True)
 
 
 def cores():
@@ -215,6 +239,27 @@ def recorded_traffic(workload, kernel):
     if r.get("kernel") != kernel or r.get("source_hash") != source_hash():
         return None
     return r.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ multi-rank aggregation
+
+def max_over_ranks(ms, world, dev):
+    """The slowest rank's time per step: the job is as slow as its slowest
+    replica (all_reduce MAX over the process group; `dev` is where the
+    reduction tensor lives: the rank's GPU under NCCL, "cpu" under gloo)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, T, ms):
+    """Whole-job tokens/s: each of the `world` replicas processes T tokens per
+    step of `ms` milliseconds (the slowest rank's time)."""
+    return world * T / (ms / 1e3)
 
 
 # ------------------------------------------------------------------ arms
@@ -327,12 +372,7 @@ def measure(layer, x, cfg, steps, warmup, world, dev, gpu_index, abi, torch, clo
     total_ms = evs[0][0].elapsed_time(evs[-1][4])
     stage_ms = {name: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / steps
                 for j, name in enumerate(["route", "permute", "expert_ffn", "combine"])}
-    ms_step = total_ms / steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / steps, world, dev)
     return dict(ms_step=ms_step, stage_ms=stage_ms, alg=alg, launches=launches, clocks=clk.summary())
 
 
@@ -364,18 +404,13 @@ def time_graph(layer, x, steps, warmup, world, dev, torch, gpu_index=None):
             dist.barrier()
         torch.cuda.synchronize(dev)
         keep_busy(graph.replay, 0.3, torch, dev)
-    ms = g0.elapsed_time(g1) / steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(g0.elapsed_time(g1) / steps, world, dev)
     return ms, clk.summary()
 
 
-# Workloads whose metric point is the tensor roofline (the T = 8192 batch and
-# the other large batches); the rest report the slower of the two bounds.
-TENSOR_WORKLOADS = ("prefill", "skew", "100b_prefill")
+# Workloads whose metric point is the tensor roofline (the two T = 8192
+# batches); the rest report the slower of the two bounds.
+TENSOR_WORKLOADS = ("prefill", "100b_prefill")
 
 
 def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_terms=2):
@@ -464,12 +499,7 @@ def run_ours(args, world, rank, local):
         layer.forward_host(x_host, y_host, x_stage, y_stage, stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     # the same layer pass replayed as one CUDA graph (no host launch gaps)
     graph_ms, graph_clk = time_graph(layer, x, args.steps, args.warmup, world, dev, torch, gpu_index)
@@ -477,50 +507,69 @@ def run_ours(args, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device status {abi.STATUS.get(st, st)}")
 
-    # the metric's second point: T = 8192 prefill on the same resident weights
-    # (the generator draws identical weights for decode and prefill)
-    second = None
+    # further points of the metric, each with its own roofline: the T = 8192
+    # prefill (the metric's second point) and the skewed batch on the same
+    # resident FP8 weights (the generator draws identical expert weights for
+    # every FP8 workload), then the 100B-style NVFP4 layer at T = 64 and 8192
+    points = {}
     if args.workload == "decode" and not args.no_prefill:
-        pin = moe_synth.make_inputs("prefill", router_only=True)
-        xp = _to_dev(pin.x, dev)
+        def point(lay, name, steps, act_terms=2, flag_note=None):
+            src = moe_synth.make_inputs(name, router_only=True)
+            if src.bias is not None:
+                import copy
+                lay = copy.copy(lay)
+                lay.bias = _to_dev(src.bias, dev)
+            xp = _to_dev(src.x, dev)
+            mp = measure(lay, xp, src.cfg, steps, args.warmup, world, dev, gpu_index, abi, torch)
+            gp, gp_clk = time_graph(lay, xp, steps, args.warmup, world, dev, torch, gpu_index)
+            rp, lfp = roofline(mp["alg"], mp["stage_ms"]["expert_ffn"], gp, name, src.cfg.w_dtype, args.simt,
+                               act_terms)
+            out = {"workload": WORKLOAD_TEXT[name], "value": job_value(world, src.cfg.T, gp), "unit": "tokens/s",
+                   "ms_per_step": gp, "steps": steps, "roofline": rp, "layer_roofline_frac": lfp,
+                   "active_experts": mp["alg"]["active"],
+                   "stream_launch": {"ms_per_step": mp["ms_step"], "stages_ms": mp["stage_ms"],
+                                     "value": job_value(world, src.cfg.T, mp["ms_step"])},
+                   "gpu_launches": int(mp["launches"]), "clocks": gp_clk}
+            if flag_note:
+                out.update(flag_note)
+            return out
+
         psteps = max(3, args.steps // 2)
-        mp = measure(layer, xp, pin.cfg, psteps, args.warmup, world, dev, gpu_index, abi, torch)
-        gp, gp_clk = time_graph(layer, xp, psteps, args.warmup, world, dev, torch, gpu_index)
-        rp, lfp = roofline(mp["alg"], mp["stage_ms"]["expert_ffn"], gp, "prefill", pin.cfg.w_dtype, args.simt)
-        second = {"workload": WORKLOAD_TEXT["prefill"], "value": world * pin.cfg.T / (gp / 1e3),
-                  "unit": "tokens/s", "ms_per_step": gp, "steps": psteps, "roofline": rp,
-                  "layer_roofline_frac": lfp,
-                  "stream_launch": {"ms_per_step": mp["ms_step"], "stages_ms": mp["stage_ms"],
-                                    "value": world * pin.cfg.T / (mp["ms_step"] / 1e3)},
-                  "gpu_launches": int(mp["launches"]), "clocks": gp_clk}
+        points["prefill"] = point(layer, "prefill", psteps)
         # the same point with the opt-in 8-bit activations (a different
         # numerical contract: see the flag's description in the header)
-        if not args.simt and not args.act_e4m3 and pin.cfg.w_dtype == "e4m3":
+        if not args.simt and not args.act_e4m3 and cfg.w_dtype == "e4m3":
             import copy
             la = copy.copy(layer)
             la.flags = layer.flags | abi.MOE_FLAG_ACT_E4M3
             la._ws = None
-            ma = measure(la, xp, pin.cfg, psteps, args.warmup, world, dev, gpu_index, abi, torch)
-            ga, ga_clk = time_graph(la, xp, psteps, args.warmup, world, dev, torch, gpu_index)
-            ra, lfa = roofline(ma["alg"], ma["stage_ms"]["expert_ffn"], ga, "prefill", pin.cfg.w_dtype, False, 1)
-            second["act_e4m3"] = {
-                "flag": "MOE_FLAG_ACT_E4M3", "value": world * pin.cfg.T / (ga / 1e3), "unit": "tokens/s",
-                "ms_per_step": ga, "roofline": ra, "layer_roofline_frac": lfa,
-                "stream_launch": {"ms_per_step": ma["ms_step"], "stages_ms": ma["stage_ms"]},
+            points["prefill"]["act_e4m3"] = point(la, "prefill", psteps, 1, {
+                "flag": "MOE_FLAG_ACT_E4M3",
                 "numerics": "one E4M3 term per activation row: parity against the oracle's restatement of that "
-                            "rounding; about 5e-2 relative L2 from exact bf16 activations",
-                "clocks": ga_clk}
+                            "rounding; about 5e-2 relative L2 from exact bf16 activations"})
+            del la
+        points["skew"] = point(layer, "skew", psteps)
+        if not args.no_100b:
+            layer = None                      # the FP8 weights are no longer needed
+            torch.cuda.empty_cache()
+            inp100 = moe_synth.make_inputs("100b_decode")
+            l100 = MoELayer(inp100, device=dev, flags=flags & ~abi.MOE_FLAG_ACT_E4M3)
+            points["100b_decode"] = point(l100, "100b_decode", args.steps)
+            points["100b_prefill"] = point(l100, "100b_prefill", psteps)
+            del l100, inp100
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
-    value = world * T / (graph_ms / 1e3)
+    value = job_value(world, T, graph_ms)
     roof, layer_frac = roofline(m["alg"], m["stage_ms"]["expert_ffn"], graph_ms, args.workload, cfg.w_dtype,
                                 args.simt, 1 if args.act_e4m3 else 2)
     cpu = None
     if not args.no_cpu_baseline and world == 1:   # the oracle baseline: rank 0 of a single-GPU run only
         v, n, el = time_oracle(inp, args.cpu_budget)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
-               "sample": f"{n} of the {T} tokens of this workload through the fp64 CPU oracle ({el:.1f} s)"}
+               "sample": f"{n} of the {T} tokens of this workload through the fp64 CPU oracle ({el:.1f} s)",
+               "single_thread": {name: oracle_one_thread(name, args.cpu_budget / 3) for name in ("tiny", "decode")}}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": graph_ms, "higher_is_better": True, "scaling": "weak",
@@ -543,17 +592,17 @@ def run_ours(args, world, rank, local):
         "timing": "each step replays the layer captured as one CUDA graph; stream_launch times the same "
                   "step launched call by call, with CUDA events between the stages; clocks are sampled while "
                   "the layer runs (the timed steps plus ~0.7 s of untimed passes around them)",
-        "stream_launch": {"ms_per_step": m["ms_step"], "value": world * T / (m["ms_step"] / 1e3),
+        "stream_launch": {"ms_per_step": m["ms_step"], "value": job_value(world, T, m["ms_step"]),
                           "stages_ms": m["stage_ms"], "clocks": m["clocks"]},
         "roofline": roof,
         "layer_roofline_frac": layer_frac,
         "active_experts": m["alg"]["active"],
         "clocks": graph_clk,
-        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_value(world, T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(), "d2h_bytes_per_step": T * d * 4},
         "gpu_launches": int(m["launches"]),
         "cpu_baseline": cpu,
-        "prefill": second,
+        **points,
     }
     print(json.dumps(line), flush=True)
 
@@ -571,11 +620,17 @@ def main():
     ap.add_argument("--act-e4m3", action="store_true",
                     help="8-bit activations (MOE_FLAG_ACT_E4M3: one E4M3 term per row, lossy; FP8 weights only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true", help="skip the T=8192 point of the decode run")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the further points of the decode run (prefill, skew, 100B decode / prefill)")
+    ap.add_argument("--no-100b", action="store_true", help="skip the 100B-style NVFP4 points of the decode run")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--oracle-sample", choices=sorted(WORKLOAD_TEXT), help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.oracle_sample:   # child process of oracle_one_thread
+        oracle_sample_main(args.oracle_sample, args.cpu_budget)
+        return
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -92,7 +92,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtyp
 typedef struct {
   int32_t T;            /* tokens, >= 0 (0 is a no-op)                          */
   int32_t d_model;      /* hidden size d: multiple of 128, <= 16384             */
-  int32_t n_experts;    /* E: 1..256                                            */
+  int32_t n_experts;    /* E: 1..256 (larger: MOE_ERR_INVALID_ARG, every call)  */
   int32_t top_k;        /* k: 1..min(E,16)                                      */
   int32_t d_ff;         /* routed expert width f: multiple of 64                */
   int32_t d_ff_shared;  /* shared expert width f_s: multiple of 64              */
@@ -198,7 +198,8 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids,
  * (MOE_NOALLOC_MAX_PAIRS = 65536 pairs x 256 experts of per-chunk counts and
  * bases); every GPU that loads the library holds it until the process exits.
  *   - Limit: T*k <= MOE_NOALLOC_MAX_PAIRS, else MOE_ERR_UNSUPPORTED is
- *     returned before anything is launched.
+ *     returned before anything is launched.  E is limited to 256 as in
+ *     every entry point (a larger E is MOE_ERR_INVALID_ARG).
  *   - The first call on a device looks up the array's device address on
  *     that device (a runtime query, no allocation); make that first call
  *     before any stream capture is begun.
@@ -261,9 +262,16 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const flo
 uint64_t moe_launch_count(void);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's status
- * word.  Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS,
- * MOE_ERR_DEVICE_NONFINITE, or MOE_ERR_CUDA if the synchronisation failed.
+ * Reads and clears the current device's status word in one atomic step,
+ * ordered after all work already queued on `stream`, then synchronises
+ * `stream` and returns what the word held: MOE_OK, MOE_ERR_DEVICE_TIMEOUT,
+ * MOE_ERR_DEVICE_BOUNDS, MOE_ERR_DEVICE_NONFINITE (the first fault recorded
+ * since the last read), or MOE_ERR_CUDA if the read or the synchronisation
+ * failed.  The word is per DEVICE, not per stream: a fault recorded by this
+ * library's kernels on any stream of the device is reported to the next
+ * reader, whichever stream it passes, and reported once.  Work still running
+ * on other streams may record a fault after the read; that fault is kept for
+ * the next read.
  */
 moe_status_t moe_get_device_status(moe_stream_t stream);
 

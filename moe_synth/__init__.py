@@ -38,7 +38,7 @@ from typing import Optional
 import numpy as np
 import torch
 
-__all__ = ["CONFIGS", "MoEInputs", "make_inputs", "bf16_bits_to_f32",
+__all__ = ["CONFIGS", "MoEInputs", "make_inputs", "make_custom", "with_heavy_tails", "bf16_bits_to_f32",
            "quantize_e4m3_rows", "quantize_nvfp4", "SKEW_C", "SKEW_DEAD"]
 
 
@@ -250,3 +250,18 @@ def make_custom(T, d, E, k, f, fs, x_dtype="f32", w_dtype="f32", seed=0, skew=Fa
     """Inputs for an ad-hoc shape (small edge-case tests)."""
     return make_inputs(MoEConfig(f"custom_T{T}_d{d}_E{E}_k{k}_f{f}", T, d, E, k, f, fs,
                                  x_dtype, w_dtype, skew), seed)
+
+
+def with_heavy_tails(inp: MoEInputs, per_row: int = 3, magnitude: float = 1000.0, seed: int = 0) -> MoEInputs:
+    """A copy of `inp` whose activations carry a heavy tail: in every token
+    row, `per_row` seeded positions are set to +-magnitude (random signs,
+    rounded to the activation dtype).  Activation outliers of this kind stretch
+    a per-row scale far above most of the row's elements."""
+    rng = np.random.default_rng(seed)
+    xf = np.array(inp.x_f32, dtype=np.float32, copy=True)
+    T, d = xf.shape
+    for t in range(T):
+        cols = rng.choice(d, size=per_row, replace=False)
+        xf[t, cols] = np.float32(magnitude) * rng.choice(np.array([-1.0, 1.0], dtype=np.float32), size=per_row)
+    x = _f32_to_bf16_bits(xf) if inp.cfg.x_dtype == "bf16" else xf
+    return dataclasses.replace(inp, x=x)

@@ -150,3 +150,14 @@ def test_test_hook_flag_is_accepted(lib):
     assert lib.moe_workspace_bytes(ctypes.byref(cfg(flags=abi.MOE_FLAG_INJECT_TIMEOUT))) > 0
     assert lib.moe_workspace_bytes(ctypes.byref(cfg(flags=abi.MOE_FLAG_BF16_EXPERT_OUT))) < \
         lib.moe_workspace_bytes(ctypes.byref(cfg()))
+
+
+def test_noalloc_permute_rejects_bad_sizes_on_the_host(lib):
+    # more than 256 experts is an invalid configuration for every entry point;
+    # more pairs than the fixed scratch holds is unsupported; both are
+    # answered before any CUDA call
+    fake = ctypes.c_void_p(0x10000)
+    big_e = cfg(T=64, n_experts=257, top_k=6)
+    assert lib.moe_permute_noalloc(ctypes.byref(big_e), fake, fake, fake, fake, None) == 1
+    too_many = cfg(T=abi.MOE_NOALLOC_MAX_PAIRS // 6 + 1, top_k=6)
+    assert lib.moe_permute_noalloc(ctypes.byref(too_many), fake, fake, fake, fake, None) == 2

@@ -60,3 +60,17 @@ def test_source_hash_covers_the_kernel_sources():
     assert len(h) == 16 and int(h, 16) >= 0
     csrc = os.path.join(bench.ROOT, "top_routed_expert_gb300", "csrc")
     assert any(fn.endswith(".cu") for fn in os.listdir(csrc))
+
+
+def test_single_rank_aggregation_is_the_identity():
+    assert bench.max_over_ranks(1.25, 1, "cpu") == 1.25
+    assert bench.job_value(1, 64, 0.5) == pytest.approx(64 / 0.5e-3)
+    assert bench.job_value(4, 64, 0.5) == pytest.approx(4 * 64 / 0.5e-3)
+
+
+def test_skew_reports_the_slower_bound():
+    # the skewed batch is not forced onto the tensor bound: HBM when bytes dominate
+    roof, _ = bench.roofline(alg(1.73e9, 0.73e12), 0.4, 0.5, "skew", "e4m3")
+    assert roof["bound"] == "hbm"
+    roof, _ = bench.roofline(alg(0.5e9, 2.0e12), 0.6, 0.7, "skew", "e4m3")
+    assert roof["bound"] == "tensor"

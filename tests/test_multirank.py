@@ -21,18 +21,17 @@ def _free_port():
 
 SCRIPT = textwrap.dedent("""
     import json, os, sys
-    import torch, torch.distributed as dist
+    import torch.distributed as dist
     sys.path.insert(0, %r)
     import bench
     dist.init_process_group("gloo")
     rank, world = dist.get_rank(), dist.get_world_size()
-    # per-rank step time differs; the job is as slow as its slowest rank
-    ms = torch.tensor([1.0 + rank])
-    dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-    T = 64
-    value = world * T / (float(ms.item()) / 1e3)
+    # per-rank step times differ; bench.py's own aggregation must report the
+    # slowest rank and the tokens of all ranks
+    ms = bench.max_over_ranks(1.0 + rank, world, "cpu")
+    value = bench.job_value(world, 64, ms)
     if rank == 0:
-        print(json.dumps({"world": world, "ms": float(ms.item()), "value": value}))
+        print(json.dumps({"world": world, "ms": ms, "value": value}))
     dist.destroy_process_group()
 """)
 

@@ -422,3 +422,59 @@ def test_act_e4m3_ffn_is_near_but_not_equal():
     # inputs already on the scaled E4M3 grid pass the first rounding unchanged
     Xq = oracle.quantize_act_rows(X)
     assert np.array_equal(oracle.quantize_act_rows(Xq), Xq)
+
+
+# --------------------------------------------------------------------------
+# The opt-in 8-bit-activation branch of swiglu_ffn, pinned as a whole: a
+# hand-worked case (tests/golden/act_e4m3_example.json) in which the bf16
+# rounding of H flips an E4M3 code, and an independent restatement with
+# torch's own float8 / bfloat16 casts and a brute-force scale search.
+
+
+def test_act_e4m3_hand_example():
+    g = _load("act_e4m3_example.json")
+    X = np.array(g["x"], dtype=np.float64)
+    W13 = np.array(g["w13"], dtype=np.float64)
+    W2 = np.array(g["w2"], dtype=np.float64)
+    ex = g["expected"]
+    assert np.array_equal(oracle.quantize_act_rows(X), np.array(ex["xq"]))
+    out = oracle.swiglu_ffn(X, W13, W2, act="e4m3")
+    assert np.allclose(out, np.array(ex["out"]), rtol=0, atol=1e-12)
+    assert not np.allclose(out, np.array(ex["out_without_bf16_rounding_of_h"]), rtol=0, atol=1e-3)
+    assert np.allclose(oracle.swiglu_ffn(X, W13, W2), np.array(ex["out_exact_activations"]), rtol=0, atol=1e-12)
+
+
+def _torch_act_rows(V):
+    """Per row: s = the smallest power of two with max|v| <= 448 s, found by
+    walking every exponent; then torch's float8_e4m3fn cast of v / s."""
+    out = torch.empty_like(V)
+    for r in range(V.shape[0]):
+        amax = float(V[r].abs().max())
+        s = 1.0
+        if amax > 0:
+            for e in range(-126, 128):
+                if amax <= 448.0 * 2.0 ** e:
+                    s = 2.0 ** e
+                    break
+        out[r] = (V[r] / s).to(torch.float8_e4m3fn).to(torch.float64) * s
+    return out
+
+
+def test_act_e4m3_ffn_matches_torch_restatement():
+    # dyadic weights keep every matmul exact in fp64, so the two sides must
+    # agree bit for bit; rows of very different magnitudes exercise the scale
+    rng = np.random.default_rng(26)
+    d, f, n = 48, 24, 10
+    X = rng.standard_normal((n, d)) * np.exp2(rng.integers(-6, 7, (n, 1)))
+    W13 = rng.integers(-64, 65, (2 * f, d)) / 256.0
+    W2 = rng.integers(-64, 65, (d, f)) / 256.0
+    got = oracle.swiglu_ffn(X, W13, W2, act="e4m3")
+    Xt, W13t, W2t = (torch.tensor(a, dtype=torch.float64) for a in (X, W13, W2))
+    Xq = _torch_act_rows(Xt)
+    G = torch.nn.functional.linear(Xq, W13t[:f])
+    U = torch.nn.functional.linear(Xq, W13t[f:])
+    H = (torch.nn.functional.silu(G) * U).to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    ref = torch.nn.functional.linear(_torch_act_rows(H), W2t).numpy()
+    assert np.array_equal(got, ref)
+    # and the rounding matters: exact activations give a different result
+    assert not np.allclose(oracle.swiglu_ffn(X, W13, W2), ref, rtol=1e-3, atol=0)

@@ -93,6 +93,37 @@ def _act_scale_doubled(amax):
 _orig_act_scale = om.act_scale
 
 
+def _swiglu_e4m3_h_not_bf16(X, W13, W2, act=None):
+    # mistake: the 8-bit branch quantises H straight from fp64
+    f = W2.shape[1]
+    if act == "e4m3":
+        X = om.quantize_act_rows(X)
+    H = om.silu(X @ W13[:f].T) * (X @ W13[f:].T)
+    if act == "e4m3":
+        H = om.quantize_act_rows(H)
+    return H @ W2.T
+
+
+def _swiglu_e4m3_h_unquantised(X, W13, W2, act=None):
+    # mistake: the 8-bit branch quantises X but leaves H at bf16
+    f = W2.shape[1]
+    if act == "e4m3":
+        X = om.quantize_act_rows(X)
+    H = om.silu(X @ W13[:f].T) * (X @ W13[f:].T)
+    if act == "e4m3":
+        H = om.round_bf16(H)
+    return H @ W2.T
+
+
+def _swiglu_e4m3_x_unquantised(X, W13, W2, act=None):
+    # mistake: the 8-bit branch quantises H only
+    f = W2.shape[1]
+    H = om.silu(X @ W13[:f].T) * (X @ W13[f:].T)
+    if act == "e4m3":
+        H = om.quantize_act_rows(om.round_bf16(H))
+    return H @ W2.T
+
+
 MUTANTS = [
     ("topk_ids", _tiebreak_high, pins.test_topk_bruteforce_with_exact_ties, (8, 3)),
     ("gates", _gates_no_renorm, pins.test_gates_special_cases, ()),
@@ -106,10 +137,16 @@ MUTANTS = [
     ("decode_e2m1_packed", _e2m1_nibbles_swapped, pins.test_e2m1_packing_nibble_order, ()),
     ("encode_e4m3", _encode_truncating, pins.test_encode_e4m3_matches_torch_cast, ()),
     ("act_scale", _act_scale_doubled, pins.test_act_scale_is_the_smallest_power_of_two, ()),
+    ("swiglu_ffn", _swiglu_e4m3_h_not_bf16, pins.test_act_e4m3_hand_example, ()),
+    ("swiglu_ffn", _swiglu_e4m3_h_not_bf16, pins.test_act_e4m3_ffn_matches_torch_restatement, ()),
+    ("swiglu_ffn", _swiglu_e4m3_h_unquantised, pins.test_act_e4m3_hand_example, ()),
+    ("swiglu_ffn", _swiglu_e4m3_h_unquantised, pins.test_act_e4m3_ffn_matches_torch_restatement, ()),
+    ("swiglu_ffn", _swiglu_e4m3_x_unquantised, pins.test_act_e4m3_hand_example, ()),
+    ("swiglu_ffn", _swiglu_e4m3_x_unquantised, pins.test_act_e4m3_ffn_matches_torch_restatement, ()),
 ]
 
 
-@pytest.mark.parametrize("name,fn,pin,args", MUTANTS, ids=[f"{m[0]}:{m[1].__name__}" for m in MUTANTS])
+@pytest.mark.parametrize("name,fn,pin,args", MUTANTS, ids=[f"{m[0]}:{m[1].__name__}:{m[2].__name__}" for m in MUTANTS])
 def test_pin_catches_mutant(monkeypatch, name, fn, pin, args):
     _patch(monkeypatch, name, fn)
     with pytest.raises(AssertionError):

@@ -41,8 +41,19 @@ cudaError_t launch_combine(const void* out_perm, const int32_t* row_of, const vo
 // Per-device status word (see moe_get_device_status).
 __device__ unsigned g_moe_status;
 
+// Where moe_get_device_status puts the value it takes out of the status
+// word: one slot per call (a host counter picks it), so that readers on
+// different host threads never share a slot unless 64 reads overlap.
+constexpr int kStatusSlots = 64;
+__device__ unsigned g_moe_status_slots[kStatusSlots];
+
+// Reads and clears the status word in one atomic step, after all earlier
+// work of the stream, and leaves the value in *slot.
+__global__ void status_take_kernel(unsigned* status, unsigned* slot) { *slot = atomicExch(status, 0u); }
+
 namespace moe {
 static std::atomic<uint64_t> g_launches{0};
+static std::atomic<uint32_t> g_status_reads{0};
 void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 }  // namespace moe
 
@@ -57,6 +68,7 @@ struct DeviceInfo {
   bool arch_ok = false;
   int num_sms = 0;
   unsigned* status = nullptr;
+  unsigned* status_slots = nullptr;
 };
 
 std::mutex g_mu;
@@ -81,6 +93,8 @@ moe_status_t device_info(DeviceInfo* out) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_moe_status) != cudaSuccess) return MOE_ERR_CUDA;
       di.status = static_cast<unsigned*>(p);
+      if (cudaGetSymbolAddress(&p, g_moe_status_slots) != cudaSuccess) return MOE_ERR_CUDA;
+      di.status_slots = static_cast<unsigned*>(p);
     }
     di.ready = true;
   }
@@ -350,13 +364,14 @@ moe_status_t moe_get_device_status(moe_stream_t stream) {
   DeviceInfo di;
   moe_status_t st = device_info(&di);
   if (st != MOE_OK) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* slot = di.status_slots + g_status_reads.fetch_add(1, std::memory_order_relaxed) % kStatusSlots;
+  count_launches(1);
+  status_take_kernel<<<1, 1, 0, s>>>(di.status, slot);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   unsigned v = 0;
-  if (cudaMemcpy(&v, di.status, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (v != 0) {
-    const unsigned zero = 0;
-    if (cudaMemcpy(di.status, &zero, sizeof(unsigned), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
-  }
+  if (cudaMemcpyAsync(&v, slot, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   return static_cast<moe_status_t>(v);
 }
 

@@ -1,7 +1,7 @@
 // Deterministic combine: y[t] = shared[t] + sum_j out_perm[row_of[t*k+j]],
 // the routed terms added in fp32 in slot order j = 0..k-1 (a gather, no
 // atomics), so the result is bitwise reproducible.  The expert outputs are
-// read as bf16 (default) or fp32.  Sarvam summary (peacm.com
+// read as fp32 (default) or as bf16 with MOE_FLAG_BF16_EXPERT_OUT.  Sarvam summary (peacm.com
 // news/791474) section 2.1: the shared expert handles common features and the
 // routed experts specific ones; their outputs are summed per token.
 #include "common.cuh"
@@ -68,7 +68,6 @@ cudaError_t launch_combine(const void* out_perm, const int32_t* row_of, const vo
       return launch_pdl(combine_kernel<float, true>, blocks, 256, 0, stream, o, row_of, sh, y, T, d, k, T * k, status);
     return launch_pdl(combine_kernel<float, false>, blocks, 256, 0, stream, o, row_of, sh, y, T, d, k, T * k, status);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace moe

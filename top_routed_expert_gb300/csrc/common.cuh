@@ -117,7 +117,7 @@ __device__ __forceinline__ float e2m1_to_float(uint32_t code) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
 
-// Expert-output element store: bf16 (default) or fp32.
+// Expert-output element store: fp32 (default) or bf16 (MOE_FLAG_BF16_EXPERT_OUT).
 __device__ __forceinline__ void store_out(void* base, size_t idx, float v, bool out_bf16) {
   if (out_bf16) static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
   else static_cast<float*>(base)[idx] = v;

@@ -12,7 +12,7 @@
 //                found with a warp match and a per-warp count table.
 // Deterministic and stable: within an expert the pairs come out in ascending
 // p, hence ascending token.  Ids outside [0, E) are skipped and recorded in
-// the device status word.
+// the device status word; their row_of entry is set to -1.
 #include <mutex>
 
 #include "common.cuh"
@@ -102,6 +102,8 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int3
       for (int w2 = 0; w2 < warp; ++w2) pos += wcnt[w2][e];
       sorted_pair[pos] = p;
       row_of[p] = pos;
+    } else if (p < end) {
+      row_of[p] = -1;   // an out-of-range id: the combine skips (and reports) this slot
     }
     __syncthreads();
     for (int i = tid; i < E; i += kPermThreads) {
@@ -160,6 +162,8 @@ permute_small_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __r
       for (int w2 = 0; w2 < warp; ++w2) pos += wcnt[w2][e];
       sorted_pair[pos] = p;
       row_of[p] = pos;
+    } else if (p < P) {
+      row_of[p] = -1;   // an out-of-range id: the combine skips (and reports) this slot
     }
     __syncthreads();
     for (int i = tid; i < E; i += kPermThreads) {
