@@ -8,4 +8,5 @@ from .moe_oracle import (E2M1_TABLE, E4M3_TABLE, decode_bf16, decode_e2m1_packed
                          decode_e4m3, dequant, expert_weights, gates, layer_forward,
                          layer_forward_tokens, near_ties, permute, route, router_logits,
                          shared_weights, silu, swiglu_ffn, topk_ids, x_values,
-                         encode_e4m3, act_scale, quantize_act_rows, round_bf16)
+                         encode_e4m3, act_scale, quantize_act_rows, round_bf16,
+                         encode_e2m1, nvfp4_row_scale, nvfp4_block_scale, quantize_nvfp4_act_rows)

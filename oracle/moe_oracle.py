@@ -245,6 +245,73 @@ def quantize_act_rows(V: np.ndarray) -> np.ndarray:
     return out
 
 
+# --------------------------------------------------------------------------
+# Optional NVFP4 activations (the W4A4 reading of the Blackwell section's
+# NVFP4 compute: activations in the same element format as the weights).
+# The opt-in W4A4 mode of the library is checked against this restatement:
+#   row scale    g = the smallest power of two (>= 2^-126) with
+#                max|v| <= 6 * 448 * g  (1 for a row without a non-zero
+#                finite maximum);
+#   block scale  per 16 consecutive elements, s = the smallest positive E4M3
+#                value with max|v_block| <= 6 * g * s  (1 for an all-zero
+#                block), so no element saturates;
+#   value        g * s * E2M1(v / (g s)), E2M1 = nearest value of
+#                {0, 0.5, 1, 1.5, 2, 3, 4, 6}, ties to the even code;
+#   H            rounded to fp32, then to bf16, before that.
+# --------------------------------------------------------------------------
+
+# non-negative E2M1 values by code 0 .. 7 (ascending with the code)
+_E2M1_POS = np.array([_e2m1_value(c) for c in range(8)], dtype=np.float64)
+
+
+def encode_e2m1(v: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 value of each element, ties to the even code, saturating
+    at +-6 (returns the values, not the codes)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    i = np.clip(np.searchsorted(_E2M1_POS, a, side="right") - 1, 0, 6)   # value(i) <= a < value(i+1)
+    lo, hi = _E2M1_POS[i], _E2M1_POS[i + 1]
+    up = (a - lo > hi - a) | ((a - lo == hi - a) & ((i & 1) == 1))
+    code = np.where(up, i + 1, i)
+    code = np.where(a >= 6.0, 7, code)
+    return np.sign(v) * _E2M1_POS[code]
+
+
+def nvfp4_row_scale(amax: float) -> float:
+    """The smallest power of two g >= 2^-126 with amax <= 6 * 448 * g."""
+    if not (amax > 0.0) or not math.isfinite(amax):
+        return 1.0
+    k = max(math.ceil(math.log2(amax / 2688.0)), -126)
+    while k > -126 and amax <= 2688.0 * 2.0 ** (k - 1):   # exact comparisons settle the log's rounding
+        k -= 1
+    while amax > 2688.0 * 2.0 ** k:
+        k += 1
+    return 2.0 ** k
+
+
+def nvfp4_block_scale(bamax: float, g: float) -> float:
+    """The smallest positive E4M3 value s with bamax <= 6 g s (1 for a zero block)."""
+    if not (bamax > 0.0):
+        return 1.0
+    i = int(np.searchsorted(_E4M3_POS * (6.0 * g), bamax, side="left"))   # first value with 6 g s >= bamax
+    return float(_E4M3_POS[min(max(i, 1), 126)])
+
+
+def quantize_nvfp4_act_rows(V: np.ndarray) -> np.ndarray:
+    """Each row v -> g s E2M1(v / (g s)) with its row scale g and the block
+    scale s of each 16 consecutive elements (the row length is a multiple
+    of 16)."""
+    V = np.asarray(V, dtype=np.float64)
+    out = np.empty_like(V)
+    for r in range(V.shape[0]):
+        g = nvfp4_row_scale(float(np.max(np.abs(V[r]))) if V.shape[1] else 0.0)
+        for b in range(0, V.shape[1], 16):
+            blk = V[r, b:b + 16]
+            sc = nvfp4_block_scale(float(np.max(np.abs(blk))), g) * g
+            out[r, b:b + 16] = encode_e2m1(blk / sc) * sc
+    return out
+
+
 def round_bf16(v: np.ndarray) -> np.ndarray:
     """float64 -> nearest fp32 -> nearest bf16 (ties to even), as float64."""
     f = np.asarray(v, dtype=np.float64).astype(np.float32)
@@ -264,18 +331,20 @@ def silu(z: np.ndarray) -> np.ndarray:
 
 def swiglu_ffn(X: np.ndarray, W13: np.ndarray, W2: np.ndarray, act: Optional[str] = None) -> np.ndarray:
     """O = (silu(X Wg^T) * (X Wu^T)) W2^T with W13 = [Wg; Wu] ([2f, d]) and
-    W2 [d, f].  act = "e4m3": the rows of X, and of H after rounding to bf16,
-    go through quantize_act_rows first."""
+    W2 [d, f].  act = "e4m3" / "nvfp4": the rows of X, and of H after
+    rounding to bf16, go through quantize_act_rows / quantize_nvfp4_act_rows
+    first."""
     f = W2.shape[1]
-    if act == "e4m3":
-        X = quantize_act_rows(X)
-    elif act is not None:
+    quant = {"e4m3": quantize_act_rows, "nvfp4": quantize_nvfp4_act_rows}
+    if act is not None and act not in quant:
         raise ValueError(act)
+    if act is not None:
+        X = quant[act](X)
     G = X @ W13[:f].T
     U = X @ W13[f:].T
     H = silu(G) * U
-    if act == "e4m3":
-        H = quantize_act_rows(round_bf16(H))
+    if act is not None:
+        H = quant[act](round_bf16(H))
     return H @ W2.T
 
 

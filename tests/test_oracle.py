@@ -478,3 +478,114 @@ def test_act_e4m3_ffn_matches_torch_restatement():
     assert np.array_equal(got, ref)
     # and the rounding matters: exact activations give a different result
     assert not np.allclose(oracle.swiglu_ffn(X, W13, W2), ref, rtol=1e-3, atol=0)
+
+
+# --------------------------------------------------------------------------
+# The opt-in NVFP4-activation branch (W4A4): each rule restated by brute
+# force, a hand-worked row (tests/golden/nvfp4_act_example.json) and the
+# whole SwiGLU composition restated independently.
+
+
+def test_nvfp4_act_hand_example():
+    g = _load("nvfp4_act_example.json")
+    row = np.array(g["row"], dtype=np.float64)
+    ex = g["expected"]
+    assert oracle.nvfp4_row_scale(float(np.abs(row).max())) == ex["g"]
+    for b, s in enumerate(ex["block_scales"]):
+        assert oracle.nvfp4_block_scale(float(np.abs(row[16 * b:16 * b + 16]).max()), ex["g"]) == s
+    got = oracle.quantize_nvfp4_act_rows(row[None])[0]
+    assert np.array_equal(got, np.array(ex["row"], dtype=np.float64))
+
+
+def _e2m1_brute(x):
+    """Nearest of the 15 E2M1 values by exhaustive search; a tie takes the
+    value whose code (magnitude index) is even; beyond 6 saturates."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    a = min(abs(x), 6.0)
+    best = min(range(8), key=lambda c: (abs(mags[c] - a), c % 2))
+    return math.copysign(mags[best], x) if mags[best] else 0.0
+
+
+def test_encode_e2m1_bruteforce():
+    rng = np.random.default_rng(31)
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    v = np.concatenate([rng.uniform(-8, 8, 4000), mids, [-m for m in mids], [0.0, 6.0, 6.5, -100.0]])
+    got = oracle.encode_e2m1(v)
+    want = np.array([_e2m1_brute(float(x)) for x in v])
+    assert np.array_equal(np.abs(got), np.abs(want)) and np.all((got == 0) | (np.sign(got) == np.sign(v)))
+
+
+def test_nvfp4_scales_bruteforce():
+    rng = np.random.default_rng(32)
+    e4m3_pos = sorted({float(x) for x in oracle.E4M3_TABLE[1:0x7F]})
+    for amax in np.concatenate([np.exp(rng.uniform(-40, 40, 300)), [2688.0, 2688.5, 1.0, 21.0]]):
+        g = oracle.nvfp4_row_scale(float(amax))
+        walk = next(2.0 ** e for e in range(-126, 128) if amax <= 2688.0 * 2.0 ** e)
+        assert g == walk
+        for frac in (1.0, 0.9, 0.31, 1e-3, 1e-6):
+            b = float(amax) * frac
+            s = oracle.nvfp4_block_scale(b, g)
+            assert s == next(v for v in e4m3_pos if b <= 6.0 * g * v)   # scan of every positive code
+    assert oracle.nvfp4_block_scale(0.0, 1.0) == 1.0 and oracle.nvfp4_row_scale(0.0) == 1.0
+
+
+def _torch_nvfp4_rows(V):
+    """Independent restatement: g by walking exponents, s by scanning the
+    E4M3 codes through torch's float8_e4m3fn view, elements by exhaustive
+    nearest-value search."""
+    codes = torch.arange(1, 0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    out = torch.empty_like(V)
+    for r in range(V.shape[0]):
+        amax = float(V[r].abs().max())
+        g = next((2.0 ** e for e in range(-126, 128) if amax <= 2688.0 * 2.0 ** e), 1.0) if amax > 0 else 1.0
+        for b in range(0, V.shape[1], 16):
+            blk = V[r, b:b + 16]
+            bm = float(blk.abs().max())
+            s = float(codes[torch.nonzero(6.0 * g * codes >= bm)[0, 0]]) if bm > 0 else 1.0
+            out[r, b:b + 16] = torch.tensor([_e2m1_brute(float(x) / (g * s)) for x in blk],
+                                            dtype=torch.float64) * (g * s)
+    return out
+
+
+def test_act_nvfp4_ffn_matches_torch_restatement():
+    # dyadic weights keep every matmul exact in fp64: bit-for-bit agreement
+    rng = np.random.default_rng(33)
+    d, f, n = 64, 32, 6
+    X = rng.standard_normal((n, d)) * np.exp2(rng.integers(-5, 6, (n, 1)))
+    W13 = rng.integers(-64, 65, (2 * f, d)) / 256.0
+    W2 = rng.integers(-64, 65, (d, f)) / 256.0
+    got = oracle.swiglu_ffn(X, W13, W2, act="nvfp4")
+    Xt, W13t, W2t = (torch.tensor(a, dtype=torch.float64) for a in (X, W13, W2))
+    Xq = _torch_nvfp4_rows(Xt)
+    G = torch.nn.functional.linear(Xq, W13t[:f])
+    U = torch.nn.functional.linear(Xq, W13t[f:])
+    H = (torch.nn.functional.silu(G) * U).to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    ref = torch.nn.functional.linear(_torch_nvfp4_rows(H), W2t).numpy()
+    assert np.array_equal(got, ref)
+    assert not np.allclose(oracle.swiglu_ffn(X, W13, W2), ref, rtol=1e-2, atol=0)
+
+
+def test_quantize_nvfp4_act_rows_error_bound():
+    # every element within half the widest E2M1 step (1) of its block scale
+    rng = np.random.default_rng(34)
+    V = rng.standard_normal((5, 256)) * np.exp(rng.uniform(-5, 5, (5, 1)))
+    Q = oracle.quantize_nvfp4_act_rows(V)
+    for r in range(5):
+        g = oracle.nvfp4_row_scale(float(np.abs(V[r]).max()))
+        for b in range(0, 256, 16):
+            s = oracle.nvfp4_block_scale(float(np.abs(V[r, b:b + 16]).max()), g)
+            assert np.all(np.abs(Q[r, b:b + 16] - V[r, b:b + 16]) <= 1.0 * g * s)
+            assert np.all(np.abs(Q[r, b:b + 16]) <= 6.0 * g * s)
+
+
+def test_act_nvfp4_swiglu_hand_example():
+    g = _load("nvfp4_swiglu_example.json")
+    d = f = 16
+    X = np.zeros((1, d))
+    X[0, 0] = g["x_col0"]
+    W13 = np.zeros((2 * f, d))
+    W13[0, 0], W13[1, 0] = g["gate_col0"]
+    W13[f, 0], W13[f + 1, 0] = g["up_col0"]
+    out = oracle.swiglu_ffn(X, W13, np.eye(d), act="nvfp4")[0, :3]
+    assert np.allclose(out, g["expected_out_first3"], rtol=0, atol=1e-12)
+    assert not np.allclose(out, g["out_without_bf16_rounding_of_h_first3"], rtol=0, atol=1e-3)

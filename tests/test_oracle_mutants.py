@@ -124,6 +124,40 @@ def _swiglu_e4m3_x_unquantised(X, W13, W2, act=None):
     return H @ W2.T
 
 
+def _e2m1_ties_away(v):
+    # mistake: ties rounded away from zero instead of to the even code
+    v = np.asarray(v, dtype=np.float64)
+    pos = om._E2M1_POS
+    a = np.minimum(np.abs(v), 6.0)
+    i = np.clip(np.searchsorted(pos, a, side="right") - 1, 0, 6)
+    up = a - pos[i] >= pos[i + 1] - a
+    return np.sign(v) * pos[np.where(up, i + 1, i)]
+
+
+def _block_scale_nearest(bamax, g):
+    # mistake: block scale rounded to the nearest E4M3 value (can saturate elements)
+    if not (bamax > 0.0):
+        return 1.0
+    t = bamax / (6.0 * g)
+    return float(om._E4M3_POS[int(np.argmin(np.abs(om._E4M3_POS[1:] - t))) + 1])
+
+
+def _row_scale_exact(amax):
+    # mistake: the row scale is amax / 2688 itself, not a power of two
+    return amax / 2688.0 if amax > 0 and math.isfinite(amax) else 1.0
+
+
+def _swiglu_nvfp4_h_not_bf16(X, W13, W2, act=None):
+    # mistake: the NVFP4 branch quantises H straight from fp64
+    f = W2.shape[1]
+    if act == "nvfp4":
+        X = om.quantize_nvfp4_act_rows(X)
+    H = om.silu(X @ W13[:f].T) * (X @ W13[f:].T)
+    if act == "nvfp4":
+        H = om.quantize_nvfp4_act_rows(H)
+    return H @ W2.T
+
+
 MUTANTS = [
     ("topk_ids", _tiebreak_high, pins.test_topk_bruteforce_with_exact_ties, (8, 3)),
     ("gates", _gates_no_renorm, pins.test_gates_special_cases, ()),
@@ -143,6 +177,13 @@ MUTANTS = [
     ("swiglu_ffn", _swiglu_e4m3_h_unquantised, pins.test_act_e4m3_ffn_matches_torch_restatement, ()),
     ("swiglu_ffn", _swiglu_e4m3_x_unquantised, pins.test_act_e4m3_hand_example, ()),
     ("swiglu_ffn", _swiglu_e4m3_x_unquantised, pins.test_act_e4m3_ffn_matches_torch_restatement, ()),
+    ("encode_e2m1", _e2m1_ties_away, pins.test_encode_e2m1_bruteforce, ()),
+    ("encode_e2m1", _e2m1_ties_away, pins.test_nvfp4_act_hand_example, ()),
+    ("nvfp4_block_scale", _block_scale_nearest, pins.test_nvfp4_scales_bruteforce, ()),
+    ("nvfp4_block_scale", _block_scale_nearest, pins.test_act_nvfp4_ffn_matches_torch_restatement, ()),
+    ("nvfp4_row_scale", _row_scale_exact, pins.test_nvfp4_act_hand_example, ()),
+    ("nvfp4_row_scale", _row_scale_exact, pins.test_act_nvfp4_ffn_matches_torch_restatement, ()),
+    ("swiglu_ffn", _swiglu_nvfp4_h_not_bf16, pins.test_act_nvfp4_swiglu_hand_example, ()),
 ]
 
 
