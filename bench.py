@@ -413,16 +413,21 @@ def time_graph(layer, x, steps, warmup, world, dev, torch, gpu_index=None):
 TENSOR_WORKLOADS = ("prefill", "100b_prefill")
 
 
-def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_terms=2):
+def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_terms=None, nvfp4_f16=False):
     """Roofline of the dominant stage (moe_expert_ffn) and of the whole layer.
 
     HBM bound: algorithmic bytes at the measured copy bandwidth.  Tensor
     bound: the layer's expert FLOPs (6*d*f per pair + 6*d*f_s per token) at
     the dense peak of the weight format (FP8 = 2x, FP4 = 4x the measured bf16
     cuBLAS rate).  `issued` adds what the tensor pipe really executes: FP8
-    weights meet two E4M3 terms per activation (2x the FLOPs at the FP8
-    rate), NVFP4 weights are rebuilt exactly in f16 (1x at the bf16 rate).
+    weights meet two E4M3 terms per activation by default (2x the FLOPs at
+    the FP8 rate) or one (MOE_FLAG_ACT_E4M3); NVFP4 weights meet four NVFP4
+    activation terms by default (4x the FLOPs at the FP4 rate) or one
+    (MOE_FLAG_ACT_NVFP4), or are rebuilt exactly in f16 (MOE_FLAG_NVFP4_F16:
+    1x at the bf16 rate).
     """
+    if act_terms is None:
+        act_terms = 4 if w_dtype == "nvfp4" else 2
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"]
     bf16 = peaks["bf16_tflops"]
@@ -442,9 +447,13 @@ def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_ter
     roof["peak_source"] = (f"{peak_src}: " + ("HBM copy GB/s" if roof["bound"] == "hbm"
                                               else f"{fmt} x bf16 cuBLAS TFLOP/s"))
     if roof["bound"] == "tensor" and not simt:
-        if w_dtype == "nvfp4":
+        if w_dtype == "nvfp4" and nvfp4_f16:
             issued = {"tflops": alg["ffn_flops"] / ffn_s / 1e12, "peak": bf16,
                       "how": "weights rebuilt exactly in f16: kind::f16 MMAs at the bf16/f16 rate"}
+        elif w_dtype == "nvfp4":
+            issued = {"tflops": act_terms * alg["ffn_flops"] / ffn_s / 1e12, "peak": tc_peak,
+                      "how": (f"{act_terms} NVFP4 terms per activation row: block-scaled kind::mxf4nvf4 MMAs issue "
+                              f"{act_terms}x the layer's FLOPs at the FP4 rate")}
         elif act_terms == 2:
             issued = {"tflops": 2.0 * alg["ffn_flops"] / ffn_s / 1e12, "peak": 2.0 * bf16,
                       "how": "two E4M3 terms per activation: kind::f8f6f4 MMAs issue 2x the FLOPs"}
@@ -513,7 +522,7 @@ def run_ours(args, world, rank, local):
     # every FP8 workload), then the 100B-style NVFP4 layer at T = 64 and 8192
     points = {}
     if args.workload == "decode" and not args.no_prefill:
-        def point(lay, name, steps, act_terms=2, flag_note=None):
+        def point(lay, name, steps, act_terms=None, flag_note=None, nvfp4_f16=False):
             src = moe_synth.make_inputs(name, router_only=True)
             if src.bias is not None:
                 import copy
@@ -523,7 +532,7 @@ def run_ours(args, world, rank, local):
             mp = measure(lay, xp, src.cfg, steps, args.warmup, world, dev, gpu_index, abi, torch)
             gp, gp_clk = time_graph(lay, xp, steps, args.warmup, world, dev, torch, gpu_index)
             rp, lfp = roofline(mp["alg"], mp["stage_ms"]["expert_ffn"], gp, name, src.cfg.w_dtype, args.simt,
-                               act_terms)
+                               act_terms, nvfp4_f16)
             out = {"workload": WORKLOAD_TEXT[name], "value": job_value(world, src.cfg.T, gp), "unit": "tokens/s",
                    "ms_per_step": gp, "steps": steps, "roofline": rp, "layer_roofline_frac": lfp,
                    "active_experts": mp["alg"]["active"],
@@ -556,6 +565,24 @@ def run_ours(args, world, rank, local):
             l100 = MoELayer(inp100, device=dev, flags=flags & ~abi.MOE_FLAG_ACT_E4M3)
             points["100b_decode"] = point(l100, "100b_decode", args.steps)
             points["100b_prefill"] = point(l100, "100b_prefill", psteps)
+            if not args.simt:
+                import copy
+                # the same points on the f16-rebuild path (exact, slower), and
+                # the prefill with one NVFP4 term per activation (W4A4, lossy)
+                lf = copy.copy(l100)
+                lf.flags = l100.flags | abi.MOE_FLAG_NVFP4_F16
+                lf._ws = None
+                points["100b_decode"]["nvfp4_f16"] = point(lf, "100b_decode", args.steps, None, {
+                    "flag": "MOE_FLAG_NVFP4_F16",
+                    "numerics": "weights rebuilt exactly in f16, row-scaled f16 activations"}, True)
+                lw = copy.copy(l100)
+                lw.flags = l100.flags | abi.MOE_FLAG_ACT_NVFP4
+                lw._ws = None
+                points["100b_prefill"]["act_nvfp4"] = point(lw, "100b_prefill", psteps, 1, {
+                    "flag": "MOE_FLAG_ACT_NVFP4",
+                    "numerics": "one NVFP4 term per activation row (W4A4): parity against the oracle's restatement "
+                                "of that rounding; about 0.1 relative L2 from exact bf16 activations"})
+                del lf, lw
             del l100, inp100
             torch.cuda.empty_cache()
 
@@ -563,7 +590,7 @@ def run_ours(args, world, rank, local):
         return
     value = job_value(world, T, graph_ms)
     roof, layer_frac = roofline(m["alg"], m["stage_ms"]["expert_ffn"], graph_ms, args.workload, cfg.w_dtype,
-                                args.simt, 1 if args.act_e4m3 else 2)
+                                args.simt, 1 if args.act_e4m3 else None)
     cpu = None
     if not args.no_cpu_baseline and world == 1:   # the oracle baseline: rank 0 of a single-GPU run only
         v, n, el = time_oracle(inp, args.cpu_budget)
@@ -575,7 +602,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": graph_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32" if args.simt else (
-            "f16 MMA with fp32 accumulate (NVFP4 weights rebuilt exactly in f16, row-scaled f16 activations, bf16 H)"
+            "e2m1 block-scaled MMA with fp32 accumulate (NVFP4 weights; four NVFP4 terms per activation row, bf16 H)"
             if cfg.w_dtype == "nvfp4" else
             "e4m3 MMA with fp32 accumulate (one-term E4M3 activations: MOE_FLAG_ACT_E4M3, lossy)" if args.act_e4m3 else
             "e4m3 MMA with fp32 accumulate (two-term E4M3 activations, bf16 H)"),

@@ -82,6 +82,24 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtyp
  * weight formats only; this is the 8-bit-activation reading of their FP8
  * compute. */
 #define MOE_FLAG_ACT_E4M3 0x8u
+/* NVFP4 activations (opt-in, lossy; W4A4).  By default NVFP4 weights run on
+ * the block-scaled FP4 tensor-core MMA with every activation row (x, and H
+ * after SwiGLU) written as a sum of four NVFP4 rows found on the residual,
+ * which stays within about 5e-5 relative L2 of the bf16 activations.  With
+ * this flag only the first term is kept: each row is scaled by
+ * g = the smallest power of two with amax <= 6 * 448 * g, every 16
+ * consecutive elements get the smallest E4M3 scale s with
+ * max|v| <= 6 g s, and each element becomes g s e2m1(v / (g s)) (nearest,
+ * ties to even); H is rounded to bf16 before that.  The MMAs then do a
+ * quarter of the work, at about 0.1 relative L2 from exact activations.
+ * Valid only with NVFP4 weights, bf16 x, widths that are multiples of 256 and
+ * at most 4096, and without MOE_FLAG_SIMT_FFN / MOE_FLAG_NVFP4_F16.  This is
+ * the FP4-activation reading of the pages' NVFP4 compute. */
+#define MOE_FLAG_ACT_NVFP4 0x10u
+/* Run NVFP4 weights on the f16 tensor-core path instead (weights rebuilt
+ * exactly in f16 in shared memory, kind::f16 MMAs); the path that also
+ * serves NVFP4 widths the block-scaled path does not take. */
+#define MOE_FLAG_NVFP4_F16 0x20u
 /* Test hook for the failure path: in the tensor-core expert GEMM, CTA 0
  * withholds one "accumulator ready" signal and every bounded wait shortens to
  * 20 ms, so the epilogue's wait runs out; the kernel drains its copies and
@@ -120,6 +138,10 @@ typedef struct {
  *              value = e2m1(code) * e4m3(block scale) * gscale.
  * Alignment: w13 / w2 / s13 / s2 16 bytes; E4M3 row scales 4 bytes; NVFP4
  * block-scale arrays 8 bytes (a misaligned pointer is MOE_ERR_INVALID_ARG).
+ * NVFP4 block-scale arrays that are 16-byte aligned (and widths that are
+ * multiples of 256, at most 4096) run on the block-scaled FP4 MMA; others
+ * run on the f16 path (see MOE_FLAG_NVFP4_F16), except with
+ * MOE_FLAG_ACT_NVFP4, where they are MOE_ERR_INVALID_ARG.
  * Source of the formats: the Sarvam summary page (peacm.com news/791474,
  * section 2.1, FP8 expert weights) and the Sarvam blog's Blackwell section
  * (NVFP4 weights).

@@ -289,12 +289,16 @@ def nvfp4_row_scale(amax: float) -> float:
     return 2.0 ** k
 
 
-def nvfp4_block_scale(bamax: float, g: float) -> float:
-    """The smallest positive E4M3 value s with bamax <= 6 g s (1 for a zero block)."""
-    if not (bamax > 0.0):
-        return 1.0
-    i = int(np.searchsorted(_E4M3_POS * (6.0 * g), bamax, side="left"))   # first value with 6 g s >= bamax
-    return float(_E4M3_POS[min(max(i, 1), 126)])
+def nvfp4_block_scale(bamax, g):
+    """The smallest positive E4M3 value s with bamax <= 6 g s (1 for a zero
+    block); elementwise over arrays of block maxima and row scales."""
+    bamax = np.asarray(bamax, dtype=np.float64)
+    six_g = 6.0 * np.asarray(g, dtype=np.float64)
+    i = np.clip(np.searchsorted(_E4M3_POS, bamax / six_g, side="left"), 1, 126)
+    # the quotient may round; the comparisons below are exact and settle it
+    i = np.where(six_g * _E4M3_POS[i] < bamax, np.minimum(i + 1, 126), i)
+    i = np.where((i > 1) & (six_g * _E4M3_POS[i - 1] >= bamax), i - 1, i)
+    return np.where(bamax > 0.0, _E4M3_POS[i], 1.0)
 
 
 def quantize_nvfp4_act_rows(V: np.ndarray) -> np.ndarray:
@@ -302,14 +306,13 @@ def quantize_nvfp4_act_rows(V: np.ndarray) -> np.ndarray:
     scale s of each 16 consecutive elements (the row length is a multiple
     of 16)."""
     V = np.asarray(V, dtype=np.float64)
-    out = np.empty_like(V)
-    for r in range(V.shape[0]):
-        g = nvfp4_row_scale(float(np.max(np.abs(V[r]))) if V.shape[1] else 0.0)
-        for b in range(0, V.shape[1], 16):
-            blk = V[r, b:b + 16]
-            sc = nvfp4_block_scale(float(np.max(np.abs(blk))), g) * g
-            out[r, b:b + 16] = encode_e2m1(blk / sc) * sc
-    return out
+    R, W = V.shape
+    if R == 0 or W == 0:
+        return V.copy()
+    g = np.array([nvfp4_row_scale(float(a)) for a in np.max(np.abs(V), axis=1)])[:, None]
+    B = V.reshape(R, W // 16, 16)
+    sc = (nvfp4_block_scale(np.max(np.abs(B), axis=2), g) * g)[:, :, None]
+    return (encode_e2m1(B / sc) * sc).reshape(R, W)
 
 
 def round_bf16(v: np.ndarray) -> np.ndarray:

@@ -99,7 +99,7 @@ def check_output(inp, y_gpu, ids_gpu, tokens=None, max_abs_rms=MAX_ABS_RMS, ulp_
     rel = np.linalg.norm(err) / np.linalg.norm(ref)
     rms = np.sqrt(np.mean(ref ** 2))
     mx = np.max(np.abs(err)) / rms
-    PARITY_LOG.append((inp.cfg.name + ("+act_e4m3" if act else ""), float(rel), float(mx)))
+    PARITY_LOG.append((inp.cfg.name + (f"+act_{act}" if act else ""), float(rel), float(mx)))
     bound = max_abs_rms * rms + ulp_rel * np.abs(ref)
     assert rel <= REL_L2 and np.all(np.abs(err) <= bound), f"rel_l2={rel:.3e} max_abs/rms={mx:.3e}"
     return rel, mx

@@ -161,3 +161,16 @@ def test_noalloc_permute_rejects_bad_sizes_on_the_host(lib):
     assert lib.moe_permute_noalloc(ctypes.byref(big_e), fake, fake, fake, fake, None) == 1
     too_many = cfg(T=abi.MOE_NOALLOC_MAX_PAIRS // 6 + 1, top_k=6)
     assert lib.moe_permute_noalloc(ctypes.byref(too_many), fake, fake, fake, fake, None) == 2
+
+
+def test_act_nvfp4_flag_validation(lib):
+    nv = dict(w_dtype=abi.MOE_NVFP4, d_ff=2048, d_ff_shared=2048, top_k=8)
+    assert lib.moe_workspace_bytes(ctypes.byref(cfg(flags=abi.MOE_FLAG_ACT_NVFP4, **nv))) > 0
+    assert lib.moe_workspace_bytes(ctypes.byref(cfg(flags=abi.MOE_FLAG_NVFP4_F16, **nv))) > 0
+    for bad in (dict(flags=abi.MOE_FLAG_ACT_NVFP4),                                   # FP8 weights
+                dict(flags=abi.MOE_FLAG_ACT_NVFP4, **dict(nv, d_ff=128)),             # width not a multiple of 256
+                dict(flags=abi.MOE_FLAG_ACT_NVFP4, **dict(nv, d_model=8192)),         # wider than 4096
+                dict(flags=abi.MOE_FLAG_ACT_NVFP4 | abi.MOE_FLAG_NVFP4_F16, **nv),
+                dict(flags=abi.MOE_FLAG_ACT_NVFP4 | abi.MOE_FLAG_SIMT_FFN, **nv),
+                dict(flags=abi.MOE_FLAG_ACT_NVFP4, x_dtype=abi.MOE_F32, **nv)):
+        assert lib.moe_workspace_bytes(ctypes.byref(cfg(**bad))) == 0, bad

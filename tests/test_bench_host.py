@@ -37,7 +37,12 @@ def test_prefill_reports_the_tensor_bound_and_issued_flops():
     assert one["issued"]["tflops"] == pytest.approx(one["achieved"])                 # one term
     fp4, _ = bench.roofline(alg(2.6e9, 3.7e12), 4.9, 5.2, "100b_prefill", "nvfp4")
     assert fp4["peak"] == pytest.approx(8000.0)                                      # FP4 = 4 x bf16
-    assert fp4["issued"]["peak"] == pytest.approx(2000.0)                            # f16 MMAs
+    assert fp4["issued"]["tflops"] == pytest.approx(4 * fp4["achieved"])             # four NVFP4 terms
+    assert fp4["issued"]["peak"] == pytest.approx(8000.0)
+    w4a4, _ = bench.roofline(alg(2.6e9, 3.7e12), 2.0, 2.2, "100b_prefill", "nvfp4", False, 1)
+    assert w4a4["issued"]["tflops"] == pytest.approx(w4a4["achieved"])               # one term
+    f16, _ = bench.roofline(alg(2.6e9, 3.7e12), 4.9, 5.2, "100b_prefill", "nvfp4", nvfp4_f16=True)
+    assert f16["issued"]["peak"] == pytest.approx(2000.0)                            # f16 MMAs
 
 
 def test_traffic_only_for_matching_sources(tmp_path, monkeypatch):

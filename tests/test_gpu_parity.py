@@ -386,3 +386,72 @@ def test_graph_capture_replays_the_layer():
     torch.cuda.synchronize()
     assert torch.equal(y, ref2)
     assert abi.moe_get_device_status() == 0
+
+
+# NVFP4 weights on the block-scaled FP4 MMA (the default for widths that are
+# multiples of 256): activations as four NVFP4 terms.  Shapes whose average
+# rows per expert select each token tile (TN = 4, 8, 16, 32; MMA N = 4 TN)
+# with ragged last tiles, f != f_s, several weight tiles per group.
+NVF4_SHAPES = [
+    dict(T=20, d=512, E=32, k=4, f=256, fs=512),     # ~2.5 rows / expert -> TN 4
+    dict(T=64, d=256, E=16, k=2, f=256, fs=256),     # 8                  -> TN 8
+    dict(T=100, d=512, E=16, k=2, f=512, fs=256),    # 12.5               -> TN 16
+    dict(T=301, d=256, E=16, k=4, f=256, fs=768),    # 75                 -> TN 32
+]
+
+
+@pytest.mark.parametrize("shape", NVF4_SHAPES, ids=[f"T{s['T']}_E{s['E']}" for s in NVF4_SHAPES])
+def test_nvfp4_block_scaled_tiles(shape):
+    inp = moe_synth.make_custom(x_dtype="bf16", w_dtype="nvfp4", seed=shape["T"] + 7, **shape)
+    _, _, y, ids, w, offs = run_layer(inp)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids)
+
+
+@pytest.mark.parametrize("name", ["100b_decode", "100b_prefill"])
+def test_nvfp4_f16_path_every_token(name):
+    # the f16-rebuild path, kept for widths the block-scaled path does not take
+    inp = workload(name)
+    _, _, y, ids, w, offs = run_layer(inp, abi.MOE_FLAG_NVFP4_F16)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids)
+
+
+def test_nvfp4_paths_agree_closely():
+    # four activation terms against the exact f16 rebuild: both within
+    # bf16-rounding distance of each other (H is rounded to bf16 in both)
+    inp = workload("100b_decode")
+    _, _, y4, ids4, _, _ = run_layer(inp, 0)
+    _, _, yh, idsh, _, _ = run_layer(inp, abi.MOE_FLAG_NVFP4_F16)
+    assert np.array_equal(ids4, idsh)
+    rel = np.linalg.norm(y4 - yh) / np.linalg.norm(yh)
+    assert rel < 3e-3, rel
+
+
+# Opt-in NVFP4 activations (MOE_FLAG_ACT_NVFP4, W4A4): parity against the
+# oracle's restatement of that rounding; the exact-activation oracle is about
+# a tenth away.
+@pytest.mark.parametrize("name", ["100b_decode", "100b_prefill"])
+def test_act_nvfp4_matches_its_oracle(name):
+    inp = workload(name)
+    _, _, y, ids, w, offs = run_layer(inp, abi.MOE_FLAG_ACT_NVFP4)
+    check_routing(inp, ids, w, offs)
+    tokens = np.arange(inp.cfg.T)
+    check_output(inp, y, ids, tokens, act="nvfp4")
+    exact = oracle_y(inp, tokens, ids[tokens])
+    rel = np.linalg.norm(y[tokens] - exact) / np.linalg.norm(exact)
+    assert 2e-2 < rel < 0.3, rel
+
+
+ACT_NVF4_SHAPES = [
+    dict(T=64, d=256, E=16, k=2, f=256, fs=512),     # 8 rows / expert -> TN 16
+    dict(T=301, d=512, E=16, k=4, f=256, fs=256),    # 75             -> TN 128
+]
+
+
+@pytest.mark.parametrize("shape", ACT_NVF4_SHAPES, ids=["T64", "T301"])
+def test_act_nvfp4_tiles(shape):
+    inp = moe_synth.make_custom(x_dtype="bf16", w_dtype="nvfp4", seed=shape["T"] + 3, **shape)
+    _, _, y, ids, w, offs = run_layer(inp, abi.MOE_FLAG_ACT_NVFP4)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids, act="nvfp4")

@@ -136,10 +136,9 @@ def _e2m1_ties_away(v):
 
 def _block_scale_nearest(bamax, g):
     # mistake: block scale rounded to the nearest E4M3 value (can saturate elements)
-    if not (bamax > 0.0):
-        return 1.0
-    t = bamax / (6.0 * g)
-    return float(om._E4M3_POS[int(np.argmin(np.abs(om._E4M3_POS[1:] - t))) + 1])
+    t = np.asarray(bamax, dtype=np.float64) / (6.0 * np.asarray(g, dtype=np.float64))
+    i = np.argmin(np.abs(om._E4M3_POS[1:][None, :] - np.reshape(t, (-1, 1))), axis=1) + 1
+    return np.where(np.asarray(bamax) > 0, om._E4M3_POS[i].reshape(np.shape(t)), 1.0)
 
 
 def _row_scale_exact(amax):

@@ -34,6 +34,11 @@ size_t ffn_fp4_ws_bytes(const moe_config_t& c);
 cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                            const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
                            void* ws, unsigned* status, int num_sms, cudaStream_t stream);
+bool ffn_nvf4_supported(const moe_config_t& c);
+size_t ffn_nvf4_ws_bytes(const moe_config_t& c);
+cudaError_t launch_ffn_nvf4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
+                            const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
+                            void* ws, unsigned* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_combine(const void* out_perm, const int32_t* row_of, const void* shared, void* y, bool in_bf16,
                            bool y_bf16, int T, int d, int k, unsigned* status, int num_sms, cudaStream_t stream);
 }  // namespace moe
@@ -117,7 +122,13 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->y_dtype != MOE_F32 && c->y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(c->T) * c->top_k > (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
   if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER | MOE_FLAG_BF16_EXPERT_OUT | MOE_FLAG_ACT_E4M3 |
-                    MOE_FLAG_INJECT_TIMEOUT)) != 0)
+                    MOE_FLAG_ACT_NVFP4 | MOE_FLAG_NVFP4_F16 | MOE_FLAG_INJECT_TIMEOUT)) != 0)
+    return MOE_ERR_INVALID_ARG;
+  // NVFP4 activations exist only on the block-scaled FP4 path
+  auto nvf4_width = [](int w) { return w % 256 == 0 && w <= 4096; };
+  if ((c->flags & MOE_FLAG_ACT_NVFP4) &&
+      (c->w_dtype != MOE_NVFP4 || c->x_dtype != MOE_BF16 || (c->flags & (MOE_FLAG_SIMT_FFN | MOE_FLAG_NVFP4_F16)) ||
+       !nvf4_width(c->d_model) || !nvf4_width(c->d_ff) || !nvf4_width(c->d_ff_shared)))
     return MOE_ERR_INVALID_ARG;
   // 8-bit activations exist only on the tensor-core FP8 path
   if ((c->flags & MOE_FLAG_ACT_E4M3) &&
@@ -135,6 +146,13 @@ bool use_fp4(const moe_config_t& c) {
   return !(c.flags & MOE_FLAG_SIMT_FFN) && ffn_fp4_supported(c);
 }
 
+// The block-scaled FP4 path, for configurations it supports (the weight
+// pointers are checked separately: its tensor maps need 16-byte aligned
+// block-scale arrays).
+bool use_nvf4(const moe_config_t& c) {
+  return !(c.flags & (MOE_FLAG_SIMT_FFN | MOE_FLAG_NVFP4_F16)) && ffn_nvf4_supported(c);
+}
+
 bool use_tc_router(const moe_config_t& c) {
   return !(c.flags & MOE_FLAG_SIMT_ROUTER) && router_tc_supported(c.T, c.d_model, c.n_experts, c.x_dtype == MOE_BF16);
 }
@@ -143,6 +161,7 @@ size_t ffn_ws_bytes(const moe_config_t& c) {
   size_t s = ffn_simt_ws_bytes(c.T, c.top_k, c.d_ff, c.d_ff_shared);
   if (use_tc(c)) s = std::max(s, ffn_tc_ws_bytes(c));
   if (use_fp4(c)) s = std::max(s, ffn_fp4_ws_bytes(c));
+  if (use_nvf4(c)) s = std::max(s, ffn_nvf4_ws_bytes(c));
   return s;
 }
 
@@ -283,6 +302,12 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float*
     return cuda_status(launch_ffn_tc(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
                                      ws, di.status, di.num_sms, s));
   if (cfg->flags & MOE_FLAG_ACT_E4M3) return MOE_ERR_UNSUPPORTED;   // no tensor-map encoder in this driver
+  const bool scales16 = aligned(weights->w13_scale, 16) && aligned(weights->w2_scale, 16) &&
+                        aligned(weights->s13_scale, 16) && aligned(weights->s2_scale, 16);
+  if (use_nvf4(*cfg) && scales16)
+    return cuda_status(launch_ffn_nvf4(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
+                                       ws, di.status, di.num_sms, s));
+  if (cfg->flags & MOE_FLAG_ACT_NVFP4) return scales16 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
   if (use_fp4(*cfg))
     return cuda_status(launch_ffn_fp4(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
                                       ws, di.status, di.num_sms, s));
