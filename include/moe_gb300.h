@@ -82,10 +82,11 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtyp
  * weight formats only; this is the 8-bit-activation reading of their FP8
  * compute. */
 #define MOE_FLAG_ACT_E4M3 0x8u
-/* NVFP4 activations (opt-in, lossy; W4A4).  By default NVFP4 weights run on
- * the block-scaled FP4 tensor-core MMA with every activation row (x, and H
- * after SwiGLU) written as a sum of four NVFP4 rows found on the residual,
- * which stays within about 5e-5 relative L2 of the bf16 activations.  With
+/* NVFP4 activations (opt-in, lossy; W4A4).  By default NVFP4 weights of a
+ * decode-sized batch run on the block-scaled FP4 tensor-core MMA with every
+ * activation row (x, and H after SwiGLU) written as a sum of four NVFP4 rows
+ * found on the residual, which stays within about 5e-5 relative L2 of the
+ * bf16 activations.  With
  * this flag only the first term is kept: each row is scaled by
  * g = the smallest power of two with amax <= 6 * 448 * g, every 16
  * consecutive elements get the smallest E4M3 scale s with
@@ -138,10 +139,12 @@ typedef struct {
  *              value = e2m1(code) * e4m3(block scale) * gscale.
  * Alignment: w13 / w2 / s13 / s2 16 bytes; E4M3 row scales 4 bytes; NVFP4
  * block-scale arrays 8 bytes (a misaligned pointer is MOE_ERR_INVALID_ARG).
- * NVFP4 block-scale arrays that are 16-byte aligned (and widths that are
- * multiples of 256, at most 4096) run on the block-scaled FP4 MMA; others
- * run on the f16 path (see MOE_FLAG_NVFP4_F16), except with
- * MOE_FLAG_ACT_NVFP4, where they are MOE_ERR_INVALID_ARG.
+ * NVFP4 batches of at most 16 routed rows per expert on average (decode)
+ * run on the block-scaled FP4 MMA when the block-scale arrays are 16-byte
+ * aligned and the widths are multiples of 256, at most 4096; other NVFP4
+ * batches run on the f16 path (see MOE_FLAG_NVFP4_F16).  With
+ * MOE_FLAG_ACT_NVFP4 every batch runs on the block-scaled MMA, and
+ * misaligned block-scale arrays are MOE_ERR_INVALID_ARG.
  * Source of the formats: the Sarvam summary page (peacm.com news/791474,
  * section 2.1, FP8 expert weights) and the Sarvam blog's Blackwell section
  * (NVFP4 weights).

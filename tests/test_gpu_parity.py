@@ -389,14 +389,15 @@ def test_graph_capture_replays_the_layer():
 
 
 # NVFP4 weights on the block-scaled FP4 MMA (the default for widths that are
-# multiples of 256): activations as four NVFP4 terms.  Shapes whose average
-# rows per expert select each token tile (TN = 4, 8, 16, 32; MMA N = 4 TN)
-# with ragged last tiles, f != f_s, several weight tiles per group.
+# multiples of 256, decode-sized batches): activations as four NVFP4 terms.
+# Shapes whose average rows per expert select each token tile (TN = 4, 8,
+# 16; MMA N = 4 TN) with ragged last tiles, f != f_s, several weight tiles per
+# group.
 NVF4_SHAPES = [
     dict(T=20, d=512, E=32, k=4, f=256, fs=512),     # ~2.5 rows / expert -> TN 4
     dict(T=64, d=256, E=16, k=2, f=256, fs=256),     # 8                  -> TN 8
     dict(T=100, d=512, E=16, k=2, f=512, fs=256),    # 12.5               -> TN 16
-    dict(T=301, d=256, E=16, k=4, f=256, fs=768),    # 75                 -> TN 32
+    dict(T=128, d=512, E=16, k=2, f=256, fs=768),    # 16 (most groups ragged) -> TN 16
 ]
 
 

@@ -35,6 +35,7 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
                            const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
                            void* ws, unsigned* status, int num_sms, cudaStream_t stream);
 bool ffn_nvf4_supported(const moe_config_t& c);
+bool ffn_nvf4_preferred(const moe_config_t& c);
 size_t ffn_nvf4_ws_bytes(const moe_config_t& c);
 cudaError_t launch_ffn_nvf4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                             const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
@@ -146,11 +147,13 @@ bool use_fp4(const moe_config_t& c) {
   return !(c.flags & MOE_FLAG_SIMT_FFN) && ffn_fp4_supported(c);
 }
 
-// The block-scaled FP4 path, for configurations it supports (the weight
-// pointers are checked separately: its tensor maps need 16-byte aligned
-// block-scale arrays).
+// The block-scaled FP4 path, for configurations it supports: always with
+// NVFP4 activations, and for the exact contract when the batch is
+// decode-sized (the weight pointers are checked separately: its tensor maps
+// need 16-byte aligned block-scale arrays).
 bool use_nvf4(const moe_config_t& c) {
-  return !(c.flags & (MOE_FLAG_SIMT_FFN | MOE_FLAG_NVFP4_F16)) && ffn_nvf4_supported(c);
+  return !(c.flags & (MOE_FLAG_SIMT_FFN | MOE_FLAG_NVFP4_F16)) && ffn_nvf4_supported(c) &&
+         ((c.flags & MOE_FLAG_ACT_NVFP4) || ffn_nvf4_preferred(c));
 }
 
 bool use_tc_router(const moe_config_t& c) {

@@ -616,7 +616,7 @@ N4Plan n4_plan(const moe_config_t& c) {
   p.total = o;
   // token rows per tile: N = terms * TN must be a multiple of 16 and at most 128
   const double avg = static_cast<double>(P) / c.n_experts;
-  if (p.terms == 4) p.TN = avg <= 4 ? 4 : avg <= 8 ? 8 : avg <= 16 ? 16 : 32;
+  if (p.terms == 4) p.TN = avg <= 4 ? 4 : avg <= 8 ? 8 : avg <= 16 ? 16 : 32;   // 32: only when forced (larger batches)
   else p.TN = avg <= 16 ? 16 : avg <= 32 ? 32 : avg <= 64 ? 64 : 128;
   return p;
 }
@@ -735,6 +735,15 @@ bool ffn_nvf4_supported(const moe_config_t& c) {
   auto ok = [](int w) { return w % 256 == 0 && w <= kN4MaxWidth; };
   return c.w_dtype == MOE_NVFP4 && c.x_dtype == MOE_BF16 && ok(c.d_model) && ok(c.d_ff) && ok(c.d_ff_shared) &&
          n4_encode_fn() != nullptr;
+}
+
+// Whether the exact (four-term) contract should take the block-scaled path:
+// yes while the routed groups are small (up to 16 rows per expert on
+// average, the decode regime, where the layer streams weights and the four
+// terms cost nothing); large batches are bound by the MMAs, which issue four
+// times the layer's FLOPs at N = 128 and are fed slower than the f16 path's.
+bool ffn_nvf4_preferred(const moe_config_t& c) {
+  return static_cast<double>(c.T) * c.top_k <= 16.0 * c.n_experts;
 }
 
 size_t ffn_nvf4_ws_bytes(const moe_config_t& c) { return n4_plan(c).total; }
