@@ -14,6 +14,14 @@ from top_routed_expert_gb300.layer import MoELayer, _to_dev
 # to the rms of the reference output).
 REL_L2 = 5e-3
 MAX_ABS_RMS = 2e-2
+# The opt-in lossy activation modes are compared with the oracle's
+# restatement of their rounding.  Both sides take the same rounding
+# decisions except where the GPU's fp32 H and the oracle's fp64 H straddle a
+# bf16 rounding boundary (about 2^-15 of the elements); such an element can
+# then move by one E4M3 / E2M1 step, or move its NVFP4 block's scale and so
+# all 16 elements of the block.  The relative-L2 bound stays; a single output
+# element may carry up to twice the default bound.
+LOSSY_MAX_ABS_RMS = 4e-2
 # Gate weights: fp32 logits carry ~1e-6 absolute error over d = 4096 terms;
 # a gate moves by about the logit error times the gate.
 GATE_ATOL = 2e-5
@@ -103,6 +111,8 @@ def check_output(inp, y_gpu, ids_gpu, tokens=None, max_abs_rms=MAX_ABS_RMS, ulp_
     rms = np.sqrt(np.mean(ref ** 2))
     mx = np.max(np.abs(err)) / rms
     PARITY_LOG.append((inp.cfg.name + (f"+act_{act}" if act else ""), float(rel), float(mx)))
+    if act is not None:
+        max_abs_rms = max(max_abs_rms, LOSSY_MAX_ABS_RMS)
     bound = max_abs_rms * rms + ulp_rel * np.abs(ref)
     assert rel <= REL_L2 and np.all(np.abs(err) <= bound), f"rel_l2={rel:.3e} max_abs/rms={mx:.3e}"
     return rel, mx

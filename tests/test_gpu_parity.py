@@ -394,8 +394,8 @@ def test_graph_capture_replays_the_layer():
 # 16; MMA N = 4 TN) with ragged last tiles, f != f_s, several weight tiles per
 # group.
 NVF4_SHAPES = [
-    dict(T=20, d=512, E=32, k=4, f=256, fs=512),     # ~2.5 rows / expert -> TN 4
-    dict(T=64, d=256, E=16, k=2, f=256, fs=256),     # 8                  -> TN 8
+    dict(T=12, d=256, E=32, k=4, f=256, fs=512),     # 1.5 rows / expert  -> TN 4
+    dict(T=20, d=512, E=32, k=4, f=256, fs=512),     # 2.5                -> TN 8
     dict(T=100, d=512, E=16, k=2, f=512, fs=256),    # 12.5               -> TN 16
     dict(T=128, d=512, E=16, k=2, f=256, fs=768),    # 16 (most groups ragged) -> TN 16
 ]

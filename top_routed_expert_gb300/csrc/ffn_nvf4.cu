@@ -428,13 +428,20 @@ ffn_nvf4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
 // the smallest power of two (>= 2^-126) with max|r| <= 6 * 448 * g; each 16
 // elements get the smallest E4M3 scale s with max|r_block| <= 6 g s (1.0 for
 // an all-zero block; every comparison exact in fp32); each element the
-// nearest e2m1 code of r / (g s), ties to even; then r -= g s e2m1.
-// One warp per row of the (P+T)-row activation space; a lane holds 8
-// consecutive elements of every 256-element chunk (a 16-element block spans
-// a lane pair).  GATHER_X: row r < P takes x[sorted_pair[r]/k], row P+t takes
-// x[t] (width d); otherwise row r of H (width f for routed rows, f_s for
-// shared rows).  Outputs, row r term t at row r*TERMS + t: packed codes
-// (element 2i in the low nibble), block-scale codes, and the row scale g.
+// nearest e2m1 code of r / (g s), ties to even; then r -= g s e2m1.  With
+// one term (the opt-in W4A4 mode, checked against an exact restatement) the
+// quotient is an IEEE division; with several terms the later terms absorb
+// any rounding of the quotient, so a reciprocal product serves.
+// One CTA of kN4QThreads threads per row of the (P+T)-row activation space;
+// a thread holds 8 consecutive elements of every kN4QThreads*8-element chunk
+// (a 16-element block spans a thread pair).  GATHER_X: row r < P takes
+// x[sorted_pair[r]/k], row P+t takes x[t] (width d); otherwise row r of H
+// (width f for routed rows, f_s for shared rows).  Outputs, row r term t at
+// row r*TERMS + t: packed codes (element 2i in the low nibble), block-scale
+// codes, and the row scale g.
+
+constexpr int kN4QThreads = 128;
+constexpr int kN4QChunk = kN4QThreads * 8;   // elements per chunk
 
 __device__ __forceinline__ float e4m3_code_value(uint32_t code) {
   const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);
@@ -465,14 +472,16 @@ __device__ __forceinline__ float nvfp4_row_scale_dev(float amax) {
 }
 
 template <bool GATHER_X, int TERMS>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kN4QThreads)
 nvf4_terms_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                   int width_r, int width_s, int src_stride, uint8_t* __restrict__ codes, int code_stride,
                   uint8_t* __restrict__ scales, int scale_stride, float* __restrict__ gsc, unsigned* status) {
   pdl_enter();
-  constexpr int kChunks = kN4MaxWidth / 256;
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  constexpr int kChunks = kN4MaxWidth / kN4QChunk;
+  constexpr int kWarps = kN4QThreads / 32;
+  __shared__ float red[TERMS][kWarps];
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (row >= P + T) return;
   const uint16_t* s;
   int width;
@@ -484,12 +493,13 @@ nvf4_terms_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ 
       t = (p >= 0 && p < P) ? p / k : -1;
     }
     if (t < 0) {   // a bad pair: zero terms (the GEMM's epilogue reports the pair)
-      if (lane == 0) set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      if (tid == 0) set_status(status, MOE_ERR_DEVICE_BOUNDS);
       for (int tt = 0; tt < TERMS; ++tt) {
         const size_t r2 = static_cast<size_t>(row) * TERMS + tt;
-        for (int cc = lane * 4; cc < width / 2; cc += 128) *reinterpret_cast<uint32_t*>(codes + r2 * code_stride + cc) = 0u;
-        for (int cc = lane; cc < width / 16; cc += 32) scales[r2 * scale_stride + cc] = 0x38u;
-        if (lane == 0) gsc[r2] = 0.f;
+        for (int cc = tid * 4; cc < width / 2; cc += 4 * kN4QThreads)
+          *reinterpret_cast<uint32_t*>(codes + r2 * code_stride + cc) = 0u;
+        for (int cc = tid; cc < width / 16; cc += kN4QThreads) scales[r2 * scale_stride + cc] = 0x38u;
+        if (tid == 0) gsc[r2] = 0.f;
       }
       return;
     }
@@ -498,12 +508,14 @@ nvf4_terms_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ 
     s = src + static_cast<size_t>(row) * src_stride;
     width = row < P ? width_r : width_s;
   }
-  const int nch = width / 256;
+  // widths are multiples of 256, so a thread pair (one 16-element block) is
+  // either wholly inside the row or wholly past it
   float r[kChunks][8];
 #pragma unroll
   for (int i = 0; i < kChunks; ++i) {
+    const int e0 = i * kN4QChunk + tid * 8;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (i < nch) v = *reinterpret_cast<const uint4*>(s + i * 256 + lane * 8);
+    if (e0 < width) v = *reinterpret_cast<const uint4*>(s + e0);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -520,6 +532,10 @@ nvf4_terms_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ 
       for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(r[i][e]));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) red[tt][warp] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) amax = fmaxf(amax, red[tt][w]);
     const float g = nvfp4_row_scale_dev(amax);
     const float six_g = 6.0f * g;
     const size_t r2 = static_cast<size_t>(row) * TERMS + tt;
@@ -527,17 +543,20 @@ nvf4_terms_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ 
     uint8_t* srow = scales + r2 * scale_stride;
 #pragma unroll
     for (int i = 0; i < kChunks; ++i) {
-      if (i < nch) {
+      const int e0 = i * kN4QChunk + tid * 8;
+      if (i * kN4QChunk < width) {               // uniform over the warp pair
         float bam = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) bam = fmaxf(bam, fabsf(r[i][e]));
         bam = fmaxf(bam, __shfl_xor_sync(0xffffffffu, bam, 1));
         const uint32_t sc = block_scale_code(bam, six_g);
         const float sv = e4m3_code_value(sc) * g;     // exact: 4 significant bits times a power of two
+        const float inv = 1.0f / sv;
         uint32_t packed = 0;
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
-          const float q0 = __fdiv_rn(r[i][e], sv), q1 = __fdiv_rn(r[i][e + 1], sv);
+          const float q0 = TERMS == 1 ? __fdiv_rn(r[i][e], sv) : r[i][e] * inv;
+          const float q1 = TERMS == 1 ? __fdiv_rn(r[i][e + 1], sv) : r[i][e + 1] * inv;
           uint16_t b;
           // the first source lands in the high nibble: element e+1 high, element e low
           asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}\n"
@@ -549,11 +568,13 @@ nvf4_terms_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ 
           r[i][e + 1] -= back.y * sv;
           packed |= static_cast<uint32_t>(b & 0xffu) << (4 * e);
         }
-        *reinterpret_cast<uint32_t*>(crow + i * 128 + lane * 4) = packed;
-        if ((lane & 1) == 0) srow[i * 16 + (lane >> 1)] = static_cast<uint8_t>(sc);
+        if (e0 < width) {
+          *reinterpret_cast<uint32_t*>(crow + e0 / 2) = packed;
+          if ((tid & 1) == 0) srow[e0 / 16] = static_cast<uint8_t>(sc);
+        }
       }
     }
-    if (lane == 0) gsc[r2] = g;
+    if (tid == 0) gsc[r2] = g;
   }
 }
 
@@ -616,7 +637,9 @@ N4Plan n4_plan(const moe_config_t& c) {
   p.total = o;
   // token rows per tile: N = terms * TN must be a multiple of 16 and at most 128
   const double avg = static_cast<double>(P) / c.n_experts;
-  if (p.terms == 4) p.TN = avg <= 4 ? 4 : avg <= 8 ? 8 : avg <= 16 ? 16 : 32;   // 32: only when forced (larger batches)
+  // (four terms: a tile about twice the average group, so that most groups
+  // of a decode batch fit one tile and each weight tile is read once)
+  if (p.terms == 4) p.TN = avg <= 2 ? 4 : avg <= 5 ? 8 : avg <= 16 ? 16 : 32;   // 32: only when forced (larger batches)
   else p.TN = avg <= 16 ? 16 : avg <= 32 ? 32 : avg <= 64 ? 64 : 128;
   return p;
 }
@@ -681,9 +704,8 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
   float* hg = reinterpret_cast<float*>(base + pl.hg);
   const uint64_t TR = static_cast<uint64_t>(R) * TERMS;
 
-  const int qblocks = ceil_div(R, 4);
   count_launches(1);
-  cudaError_t err = launch_pdl(nvf4_terms_kernel<true, TERMS>, qblocks, 128, 0, stream, static_cast<const uint16_t*>(x),
+  cudaError_t err = launch_pdl(nvf4_terms_kernel<true, TERMS>, R, kN4QThreads, 0, stream, static_cast<const uint16_t*>(x),
                                sorted_pair, P, T, k, d, d, d, xq, d / 2, xs, d / 16, xg, status);
   if (err != cudaSuccess) return err;
 
@@ -709,7 +731,7 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
   if (err != cudaSuccess) return err;
 
   count_launches(1);
-  err = launch_pdl(nvf4_terms_kernel<false, TERMS>, qblocks, 128, 0, stream, reinterpret_cast<const uint16_t*>(h),
+  err = launch_pdl(nvf4_terms_kernel<false, TERMS>, R, kN4QThreads, 0, stream, reinterpret_cast<const uint16_t*>(h),
                    static_cast<const int32_t*>(nullptr), P, T, k, f, fs, fmax, hq, fmax / 2, hs, fmax / 16, hg, status);
   if (err != cudaSuccess) return err;
 
