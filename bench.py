@@ -512,6 +512,15 @@ def run_ours(args, world, rank, local):
 
     # the same layer pass replayed as one CUDA graph (no host launch gaps)
     graph_ms, graph_clk = time_graph(layer, x, args.steps, args.warmup, world, dev, torch, gpu_index)
+    # and with the shared expert in the routed launches instead of beside the
+    # routing on a second stream (MOE_FLAG_NO_OVERLAP), for comparison
+    one_stream_ms = None
+    if not args.simt:
+        import copy
+        l1 = copy.copy(layer)
+        l1.flags = layer.flags | abi.MOE_FLAG_NO_OVERLAP
+        one_stream_ms, _ = time_graph(l1, x, args.steps, args.warmup, world, dev, torch, None)
+        del l1
     st = abi.moe_get_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {abi.STATUS.get(st, st)}")
@@ -531,6 +540,12 @@ def run_ours(args, world, rank, local):
             xp = _to_dev(src.x, dev)
             mp = measure(lay, xp, src.cfg, steps, args.warmup, world, dev, gpu_index, abi, torch)
             gp, gp_clk = time_graph(lay, xp, steps, args.warmup, world, dev, torch, gpu_index)
+            g1 = None
+            if not args.simt:
+                import copy
+                l1 = copy.copy(lay)
+                l1.flags = lay.flags | abi.MOE_FLAG_NO_OVERLAP
+                g1, _ = time_graph(l1, xp, steps, args.warmup, world, dev, torch, None)
             rp, lfp = roofline(mp["alg"], mp["stage_ms"]["expert_ffn"], gp, name, src.cfg.w_dtype, args.simt,
                                act_terms, nvfp4_f16)
             out = {"workload": WORKLOAD_TEXT[name], "value": job_value(world, src.cfg.T, gp), "unit": "tokens/s",
@@ -538,7 +553,8 @@ def run_ours(args, world, rank, local):
                    "active_experts": mp["alg"]["active"],
                    "stream_launch": {"ms_per_step": mp["ms_step"], "stages_ms": mp["stage_ms"],
                                      "value": job_value(world, src.cfg.T, mp["ms_step"])},
-                   "gpu_launches": int(mp["launches"]), "clocks": gp_clk}
+                   "gpu_launches": int(mp["launches"]), "clocks": gp_clk,
+                   "one_stream_ms_per_step": g1}
             if flag_note:
                 out.update(flag_note)
             return out
@@ -616,13 +632,16 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (no flush needed): the expert stage moves %.2f GB per pass, "
                          "the expert weights alone over 1.5 GB" % (m["alg"]["ffn_bytes"] / 1e9)},
-        "timing": "each step replays the layer captured as one CUDA graph; stream_launch times the same "
-                  "step launched call by call, with CUDA events between the stages; clocks are sampled while "
+        "timing": "each step replays the layer (moe_layer_forward: the shared expert on a second stream beside "
+                  "the routing) captured as one CUDA graph; one_stream_ms_per_step replays it with "
+                  "MOE_FLAG_NO_OVERLAP (everything on one stream); stream_launch times the same step as the four "
+                  "ABI calls launched one by one, with CUDA events between the stages; clocks are sampled while "
                   "the layer runs (the timed steps plus ~0.7 s of untimed passes around them)",
         "stream_launch": {"ms_per_step": m["ms_step"], "value": job_value(world, T, m["ms_step"]),
                           "stages_ms": m["stage_ms"], "clocks": m["clocks"]},
         "roofline": roof,
         "layer_roofline_frac": layer_frac,
+        "one_stream_ms_per_step": one_stream_ms,
         "active_experts": m["alg"]["active"],
         "clocks": graph_clk,
         "e2e": {"value": job_value(world, T, e2e_ms), "unit": "tokens/s",

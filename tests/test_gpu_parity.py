@@ -456,3 +456,32 @@ def test_act_nvfp4_tiles(shape):
     _, _, y, ids, w, offs = run_layer(inp, abi.MOE_FLAG_ACT_NVFP4)
     check_routing(inp, ids, w, offs)
     check_output(inp, y, ids, act="nvfp4")
+
+
+# The shared expert beside the routing (a second stream inside
+# moe_layer_forward) changes no arithmetic: the same bits as the layer with
+# everything on one stream, on each FFN path.
+@pytest.mark.parametrize("name,flags", [("decode", 0), ("prefill", 0), ("100b_decode", 0),
+                                        ("100b_prefill", 0), ("decode", abi.MOE_FLAG_ACT_E4M3),
+                                        ("100b_decode", abi.MOE_FLAG_ACT_NVFP4)])
+def test_shared_expert_overlap_is_bitwise_neutral(name, flags):
+    inp = workload(name)
+    x = device_x(inp)
+    y_split = MoELayer(inp, flags=flags).forward(x).clone()
+    y_one = MoELayer(inp, flags=flags | abi.MOE_FLAG_NO_OVERLAP).forward(x)
+    assert abi.moe_get_device_status() == 0
+    assert torch.equal(y_split, y_one)
+
+
+def test_overlapped_layer_captures_and_replays():
+    # the fork and join record into the graph; replays track new inputs
+    inp = workload("100b_decode")
+    layer = MoELayer(inp)
+    x = device_x(inp)
+    graph, y = layer.capture(x)
+    x.copy_(torch.roll(x, 3, dims=0))
+    graph.replay()
+    torch.cuda.synchronize()
+    ref = MoELayer(inp, flags=abi.MOE_FLAG_NO_OVERLAP).forward(x)
+    assert torch.equal(y, ref)
+    assert abi.moe_get_device_status() == 0

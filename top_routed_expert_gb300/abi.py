@@ -23,6 +23,7 @@ MOE_FLAG_BF16_EXPERT_OUT = 0x4
 MOE_FLAG_ACT_E4M3 = 0x8
 MOE_FLAG_ACT_NVFP4 = 0x10
 MOE_FLAG_NVFP4_F16 = 0x20
+MOE_FLAG_NO_OVERLAP = 0x40
 MOE_FLAG_INJECT_TIMEOUT = 0x100
 MOE_NOALLOC_MAX_PAIRS = 65536
 

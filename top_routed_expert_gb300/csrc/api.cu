@@ -28,18 +28,18 @@ bool ffn_tc_supported(const moe_config_t& c);
 size_t ffn_tc_ws_bytes(const moe_config_t& c);
 cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                           const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
-                          void* ws, unsigned* status, int num_sms, cudaStream_t stream);
+                          void* ws, unsigned* status, int num_sms, const FfnPart& part, cudaStream_t stream);
 bool ffn_fp4_supported(const moe_config_t& c);
 size_t ffn_fp4_ws_bytes(const moe_config_t& c);
 cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                            const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
-                           void* ws, unsigned* status, int num_sms, cudaStream_t stream);
+                           void* ws, unsigned* status, int num_sms, const FfnPart& part, cudaStream_t stream);
 bool ffn_nvf4_supported(const moe_config_t& c);
 bool ffn_nvf4_preferred(const moe_config_t& c);
 size_t ffn_nvf4_ws_bytes(const moe_config_t& c);
 cudaError_t launch_ffn_nvf4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                             const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
-                            void* ws, unsigned* status, int num_sms, cudaStream_t stream);
+                            void* ws, unsigned* status, int num_sms, const FfnPart& part, cudaStream_t stream);
 cudaError_t launch_combine(const void* out_perm, const int32_t* row_of, const void* shared, void* y, bool in_bf16,
                            bool y_bf16, int T, int d, int k, unsigned* status, int num_sms, cudaStream_t stream);
 }  // namespace moe
@@ -75,10 +75,15 @@ struct DeviceInfo {
   int num_sms = 0;
   unsigned* status = nullptr;
   unsigned* status_slots = nullptr;
+  // the layer's second stream (the shared expert beside the routing) and its
+  // fork / join events; created with the device's first call
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
+std::mutex g_side_mu[kMaxDevices];   // one fork / join sequence at a time per device
 
 // Looks up (once per device) the SM count, the architecture and the status
 // word address of the current device.
@@ -101,6 +106,10 @@ moe_status_t device_info(DeviceInfo* out) {
       di.status = static_cast<unsigned*>(p);
       if (cudaGetSymbolAddress(&p, g_moe_status_slots) != cudaSuccess) return MOE_ERR_CUDA;
       di.status_slots = static_cast<unsigned*>(p);
+      if (cudaStreamCreateWithFlags(&di.side, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&di.fork, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&di.join, cudaEventDisableTiming) != cudaSuccess)
+        return MOE_ERR_CUDA;
     }
     di.ready = true;
   }
@@ -123,7 +132,7 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->y_dtype != MOE_F32 && c->y_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(c->T) * c->top_k > (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
   if ((c->flags & ~(MOE_FLAG_SIMT_FFN | MOE_FLAG_SIMT_ROUTER | MOE_FLAG_BF16_EXPERT_OUT | MOE_FLAG_ACT_E4M3 |
-                    MOE_FLAG_ACT_NVFP4 | MOE_FLAG_NVFP4_F16 | MOE_FLAG_INJECT_TIMEOUT)) != 0)
+                    MOE_FLAG_ACT_NVFP4 | MOE_FLAG_NVFP4_F16 | MOE_FLAG_NO_OVERLAP | MOE_FLAG_INJECT_TIMEOUT)) != 0)
     return MOE_ERR_INVALID_ARG;
   // NVFP4 activations exist only on the block-scaled FP4 path
   auto nvf4_width = [](int w) { return w % 256 == 0 && w <= 4096; };
@@ -168,9 +177,12 @@ size_t ffn_ws_bytes(const moe_config_t& c) {
   return s;
 }
 
-// Workspace layout of moe_layer_forward.
+// Workspace layout of moe_layer_forward.  The routing scratch (tensor-core
+// router planes, permutation counts) and the expert-FFN scratch are
+// separate, so that the shared expert can run beside the routing on a
+// second stream.
 struct FwdPlan {
-  size_t ids, w, offsets, sorted_pair, row_of, out_perm, shared_out, scratch, total;
+  size_t ids, w, offsets, sorted_pair, row_of, out_perm, shared_out, route_scratch, scratch, total;
 };
 
 FwdPlan plan_forward(const moe_config_t& c) {
@@ -186,9 +198,10 @@ FwdPlan plan_forward(const moe_config_t& c) {
   const size_t esz = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) ? 2 : 4;   // expert-output element size
   p.out_perm = take(esz * P * c.d_model);
   p.shared_out = take(esz * static_cast<size_t>(c.T) * c.d_model);
-  size_t scratch = std::max(permute_ws_bytes(static_cast<int>(P), c.n_experts), ffn_ws_bytes(c));
-  if (use_tc_router(c)) scratch = std::max(scratch, router_tc_ws_bytes(c.d_model));
-  p.scratch = take(scratch);
+  size_t route = permute_ws_bytes(static_cast<int>(P), c.n_experts);
+  if (use_tc_router(c)) route = std::max(route, router_tc_ws_bytes(c.d_model));
+  p.route_scratch = take(route);
+  p.scratch = take(ffn_ws_bytes(c));
   p.total = o;
   return p;
 }
@@ -210,6 +223,62 @@ bool weights_ok(const moe_config_t& c, const moe_weights_t* w) {
     if (!w->w13_gscale || !w->w2_gscale || !w->s13_gscale || !w->s2_gscale) return false;
   }
   return true;
+}
+
+// Which FFN kernels a validated configuration runs; kSimt cannot be split.
+enum FfnPath { kFp8Tc, kNvf4, kFp4F16, kSimt, kUnsupported };
+
+FfnPath ffn_path(const moe_config_t& c, const moe_weights_t* w) {
+  if (use_tc(c)) return kFp8Tc;
+  if (c.flags & MOE_FLAG_ACT_E4M3) return kUnsupported;   // no tensor-map encoder in this driver
+  const bool scales16 = aligned(w->w13_scale, 16) && aligned(w->w2_scale, 16) && aligned(w->s13_scale, 16) &&
+                        aligned(w->s2_scale, 16);
+  if (use_nvf4(c) && scales16) return kNvf4;
+  if (c.flags & MOE_FLAG_ACT_NVFP4) return kUnsupported;
+  if (use_fp4(c)) return kFp4F16;
+  return kSimt;
+}
+
+// The expert FFN (routed experts, shared expert, or both: `part`) on the
+// kernels the configuration selects.  Arguments are already validated.
+moe_status_t run_expert_ffn(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
+                            const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
+                            void* ws, const DeviceInfo& di, const FfnPart& part, cudaStream_t s) {
+  switch (ffn_path(c, w)) {
+    case kFp8Tc:
+      return cuda_status(launch_ffn_tc(c, x, topk_w, offsets, sorted_pair, w, out_perm, shared_out, ws, di.status,
+                                       di.num_sms, part, s));
+    case kNvf4:
+      return cuda_status(launch_ffn_nvf4(c, x, topk_w, offsets, sorted_pair, w, out_perm, shared_out, ws, di.status,
+                                         di.num_sms, part, s));
+    case kFp4F16:
+      return cuda_status(launch_ffn_fp4(c, x, topk_w, offsets, sorted_pair, w, out_perm, shared_out, ws, di.status,
+                                        di.num_sms, part, s));
+    case kSimt:
+      if (!part.routed || !part.shared) return MOE_ERR_UNSUPPORTED;
+      return cuda_status(launch_ffn_simt(x, c.x_dtype == MOE_BF16, c.w_dtype, topk_w, offsets, sorted_pair, w,
+                                         out_perm, shared_out, (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0, c.T,
+                                         c.d_model, c.n_experts, c.top_k, c.d_ff, c.d_ff_shared, ws, di.status, s));
+    default:
+      break;
+  }
+  const bool scales16 = aligned(w->w13_scale, 16) && aligned(w->w2_scale, 16) && aligned(w->s13_scale, 16) &&
+                        aligned(w->s2_scale, 16);
+  return (c.flags & MOE_FLAG_ACT_NVFP4) && !scales16 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+}
+
+// SMs given to the shared expert when it runs beside the routing: its share
+// of the expert work -- of the weight bytes while the routed groups are
+// decode-sized (the FFN streams weights), of the FLOPs for larger batches
+// (the FFN is bound by the MMAs) -- so that both halves end together; at
+// least 4, at most half the GPU.
+int shared_expert_sms(const moe_config_t& c, int num_sms) {
+  const double P = static_cast<double>(c.T) * c.top_k, fs = c.d_ff_shared;
+  double frac;
+  if (P <= 16.0 * c.n_experts) frac = fs / (std::min<double>(c.n_experts, P) * c.d_ff + fs);
+  else frac = static_cast<double>(c.T) * fs / (P * c.d_ff + c.T * fs);
+  const int sms = static_cast<int>(frac * num_sms + 0.5);
+  return std::max(std::min(sms, num_sms / 2), std::min(4, num_sms / 2));
 }
 
 }  // namespace
@@ -300,24 +369,8 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x, const float*
   if (!aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
   DeviceInfo di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (use_tc(*cfg))
-    return cuda_status(launch_ffn_tc(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
-                                     ws, di.status, di.num_sms, s));
-  if (cfg->flags & MOE_FLAG_ACT_E4M3) return MOE_ERR_UNSUPPORTED;   // no tensor-map encoder in this driver
-  const bool scales16 = aligned(weights->w13_scale, 16) && aligned(weights->w2_scale, 16) &&
-                        aligned(weights->s13_scale, 16) && aligned(weights->s2_scale, 16);
-  if (use_nvf4(*cfg) && scales16)
-    return cuda_status(launch_ffn_nvf4(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
-                                       ws, di.status, di.num_sms, s));
-  if (cfg->flags & MOE_FLAG_ACT_NVFP4) return scales16 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
-  if (use_fp4(*cfg))
-    return cuda_status(launch_ffn_fp4(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out,
-                                      ws, di.status, di.num_sms, s));
-  return cuda_status(launch_ffn_simt(x, cfg->x_dtype == MOE_BF16, cfg->w_dtype, topk_w, expert_offsets,
-                                     sorted_pair, weights, out_perm, shared_out,
-                                     (cfg->flags & MOE_FLAG_BF16_EXPERT_OUT) != 0, cfg->T, cfg->d_model,
-                                     cfg->n_experts, cfg->top_k, cfg->d_ff, cfg->d_ff_shared, ws, di.status, s));
+  return run_expert_ffn(*cfg, x, topk_w, expert_offsets, sorted_pair, weights, out_perm, shared_out, ws, di,
+                        FfnPart(), static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* out_perm, const int32_t* row_of,
@@ -363,16 +416,53 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const flo
   int32_t* row_of = reinterpret_cast<int32_t*>(base + p.row_of);
   void* out_perm = base + p.out_perm;
   void* shared_out = base + p.shared_out;
+  void* rscratch = base + p.route_scratch;
+  const size_t rscratch_bytes = p.scratch - p.route_scratch;
   void* scratch = base + p.scratch;
   const size_t scratch_bytes = p.total - p.scratch;
-  if ((st = moe_route(cfg, x, w_router, expert_bias, ids, w, scratch, scratch_bytes, stream)) != MOE_OK) return st;
-  if ((st = moe_permute(cfg, ids, offsets, sorted_pair, row_of, scratch, scratch_bytes, stream)) != MOE_OK)
-    return st;
-  if ((st = moe_expert_ffn(cfg, x, w, offsets, sorted_pair, weights, out_perm, shared_out, scratch, scratch_bytes,
-                           stream)) != MOE_OK)
-    return st;
-  if ((st = moe_combine(cfg, out_perm, row_of, shared_out, y, stream)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceInfo di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const FfnPath path = ffn_path(*cfg, weights);
+  if ((cfg->flags & MOE_FLAG_NO_OVERLAP) || path == kSimt || path == kUnsupported || !di.side) {
+    if ((st = moe_route(cfg, x, w_router, expert_bias, ids, w, rscratch, rscratch_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_permute(cfg, ids, offsets, sorted_pair, row_of, rscratch, rscratch_bytes, stream)) != MOE_OK)
+      return st;
+    if ((st = moe_expert_ffn(cfg, x, w, offsets, sorted_pair, weights, out_perm, shared_out, scratch, scratch_bytes,
+                             stream)) != MOE_OK)
+      return st;
+  } else {
+    // The shared expert needs no routing result (Sarvam blog, "hiding
+    // latency by overlap": the shared expert runs on a second CUDA stream
+    // while the router logits and top-k are computed).  Fork the library's
+    // side stream off `stream`, run the shared expert there on its share of
+    // the SMs, run route -> permute -> routed experts on the rest, and join
+    // before the combine.  The two parts touch disjoint rows of the FFN
+    // scratch; the routing has scratch of its own.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_side_mu[dev]);
+    const int sh = shared_expert_sms(*cfg, di.num_sms);
+    FfnPart shared_part, routed_part;
+    shared_part.routed = false;
+    shared_part.grid_cap = sh;
+    routed_part.shared = false;
+    routed_part.grid_cap = di.num_sms - sh;
+    if (cudaEventRecord(di.fork, s) != cudaSuccess || cudaStreamWaitEvent(di.side, di.fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    st = run_expert_ffn(*cfg, x, w, offsets, sorted_pair, weights, out_perm, shared_out, scratch, di, shared_part,
+                        di.side);
+    // the join is recorded and awaited on every path, so a capture stays whole
+    const bool joined = cudaEventRecord(di.join, di.side) == cudaSuccess;
+    if (st == MOE_OK) st = moe_route(cfg, x, w_router, expert_bias, ids, w, rscratch, rscratch_bytes, stream);
+    if (st == MOE_OK) st = moe_permute(cfg, ids, offsets, sorted_pair, row_of, rscratch, rscratch_bytes, stream);
+    if (st == MOE_OK)
+      st = run_expert_ffn(*cfg, x, w, offsets, sorted_pair, weights, out_perm, shared_out, scratch, di, routed_part,
+                          s);
+    if (!joined || cudaStreamWaitEvent(s, di.join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (st != MOE_OK) return st;
+  }
+  if ((st = moe_combine(cfg, out_perm, row_of, shared_out, y, stream)) != MOE_OK) return st;
   const size_t P = static_cast<size_t>(cfg->T) * cfg->top_k;
   if (topk_ids_opt &&
       cudaMemcpyAsync(topk_ids_opt, ids, sizeof(int32_t) * P, cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -50,6 +50,17 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 
 constexpr int kMaxExperts = 256;
+
+// Which part of the expert FFN one set of launches computes: the routed
+// experts (activation rows [0, P)), the shared expert (rows [P, P+T)), or
+// both; and the most CTAs its persistent GEMMs may use (the rest of the GPU
+// stays free for work running beside them on another stream).
+struct FfnPart {
+  bool routed = true, shared = true;
+  int grid_cap = 1 << 30;
+  int row_begin(int P) const { return routed ? 0 : P; }
+  int row_end(int P, int T) const { return shared ? P + T : P; }
+};
 constexpr int kMaxGroups = kMaxExperts + 1;   // routed experts + the shared expert
 
 // Host-side count of kernel launches (moe_launch_count); defined in api.cu.

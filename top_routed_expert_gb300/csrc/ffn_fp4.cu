@@ -70,6 +70,7 @@ struct F4Args {
   void* shared_out;           // gemm2 out [T][d]
   bool out_bf16;
   int T, k, E, P, d, f, fs, fmax;
+  int routed_on, shared_on;   // which groups this launch computes (FfnPart)
   int TN, stages, bslots, raw_slots, acc_bufs, tmem_cols;
   unsigned* status;
 };
@@ -236,8 +237,12 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
     fence_barrier_init();
   }
   pdl_enter();   // from here on the kernel reads what earlier kernels wrote
-  if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kF4BM, a.fs / kF4BM, a.status);
-  else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kF4BM, a.d / kF4BM, a.status);
+  if (MODE == 1)
+    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN,
+                      a.routed_on ? a.f / kF4BM : 0, a.shared_on ? a.fs / kF4BM : 0, a.status);
+  else
+    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN,
+                      a.routed_on ? a.d / kF4BM : 0, a.shared_on ? a.d / kF4BM : 0, a.status);
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
     tmem_relinquish();
@@ -512,18 +517,18 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
 
 // Row scaler: f16 copy of an activation row divided by s = 2^(e-14), where
 // amax = m 2^e (m in [0.5,1)), so the row's largest magnitude is m 2^14.
-// One warp per row of the (P+T)-row space; GATHER_X takes row r < P from
-// x[sorted_pair[r]/k] and row P+t from x[t], else row r of H (width f for
-// routed rows, f_s for shared rows).
+// One warp per row of the (P+T)-row space, rows [row_begin, row_end);
+// GATHER_X takes row r < P from x[sorted_pair[r]/k] and row P+t from x[t],
+// else row r of H (width f for routed rows, f_s for shared rows).
 template <bool GATHER_X, bool IN_REGS>
 __global__ void __launch_bounds__(256)
 scale16_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                     int width_r, int width_s, int src_stride, __half* __restrict__ dst, int dst_stride,
-                    float* __restrict__ scale, unsigned* status) {
+                    float* __restrict__ scale, int row_begin, int row_end, unsigned* status) {
   pdl_enter();
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int row = row_begin + blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= P + T) return;
+  if (row >= row_end) return;
   __half* drow = dst + static_cast<size_t>(row) * dst_stride;
   const uint16_t* s;
   int width;
@@ -671,7 +676,7 @@ F4Plan f4_plan(const moe_config_t& c) {
 
 template <int MODE>
 cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const CUtensorMap& mAs, F4Args a,
-                           int wtiles_max, int num_sms, cudaStream_t stream) {
+                           int wtiles_routed, int wtiles_shared, int grid_cap, cudaStream_t stream) {
   constexpr int NA = (MODE == 1) ? 2 : 1;
   const int N = a.TN;
   const int stage_bytes = NA * kF4ATile;
@@ -699,9 +704,9 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
   if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_fp4_kernel<MODE>), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  const long long tiles_ub =
-      static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
+  const long long tiles_ub = (a.routed_on ? static_cast<long long>(wtiles_routed) * (a.P / a.TN + a.E) : 0) +
+                             (a.shared_on ? static_cast<long long>(wtiles_shared) * ((a.T + a.TN - 1) / a.TN) : 0);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(grid_cap, tiles_ub)));
   count_launches(1);
   return launch_pdl(ffn_fp4_kernel<MODE>, grid, kF4Threads, smem, stream, mB, mA, mAs, a);
 }
@@ -717,7 +722,7 @@ size_t ffn_fp4_ws_bytes(const moe_config_t& c) { return f4_plan(c).total; }
 
 cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                            const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
-                           void* ws, unsigned* status, int num_sms, cudaStream_t stream) {
+                           void* ws, unsigned* status, int num_sms, const FfnPart& part, cudaStream_t stream) {
   const int T = c.T, k = c.top_k, E = c.n_experts, d = c.d_model, f = c.d_ff, fs = c.d_ff_shared;
   if (T == 0) return cudaSuccess;
   const int P = T * k, R = P + T;
@@ -730,12 +735,14 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   __half* hh = reinterpret_cast<__half*>(base + pl.hh);
   float* sh = reinterpret_cast<float*>(base + pl.sh);
 
-  const int qblocks = ceil_div(R, 8);
+  const int r0 = part.row_begin(P), r1 = part.row_end(P, T);
+  const int qblocks = ceil_div(r1 - r0, 8);
   const bool regs = R <= 4096;   // see the FP8 path: registers for few rows, two passes for many
+  const int cap = std::min(num_sms, part.grid_cap);
   count_launches(1);
   cudaError_t err = launch_pdl(regs ? scale16_rows_kernel<true, true> : scale16_rows_kernel<true, false>, qblocks, 256,
                                0, stream, static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d, d, d, xh, d, sx,
-                               status);
+                               r0, r1, status);
   if (err != cudaSuccess) return err;
 
   F4Args a = {};
@@ -743,6 +750,7 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   a.h = h; a.out_perm = out_perm; a.shared_out = shared_out;
   a.out_bf16 = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0;
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
+  a.routed_on = part.routed; a.shared_on = part.shared;
   a.TN = pl.TN; a.status = status;
 
   CUtensorMap mB, mA, mAs;
@@ -754,13 +762,13 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   a.wsc = static_cast<const uint8_t*>(w->w13_scale); a.wg = w->w13_gscale;
   a.ssc = static_cast<const uint8_t*>(w->s13_scale); a.sg = w->s13_gscale;
   a.b_scale = sx;
-  err = launch_f4_gemm<1>(mB, mA, mAs, a, fmax / kF4BM, num_sms, stream);
+  err = launch_f4_gemm<1>(mB, mA, mAs, a, f / kF4BM, fs / kF4BM, cap, stream);
   if (err != cudaSuccess) return err;
 
   count_launches(1);
   err = launch_pdl(regs ? scale16_rows_kernel<false, true> : scale16_rows_kernel<false, false>, qblocks, 256, 0,
                    stream, reinterpret_cast<const uint16_t*>(h), static_cast<const int32_t*>(nullptr), P, T, k, f, fs,
-                   fmax, hh, fmax, sh, status);
+                   fmax, hh, fmax, sh, r0, r1, status);
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs
@@ -771,7 +779,7 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   a.wsc = static_cast<const uint8_t*>(w->w2_scale); a.wg = w->w2_gscale;
   a.ssc = static_cast<const uint8_t*>(w->s2_scale); a.sg = w->s2_gscale;
   a.b_scale = sh;
-  return launch_f4_gemm<2>(mB, mA, mAs, a, d / kF4BM, num_sms, stream);
+  return launch_f4_gemm<2>(mB, mA, mAs, a, d / kF4BM, d / kF4BM, cap, stream);
 }
 
 }  // namespace moe

@@ -72,6 +72,7 @@ struct N4Args {
   void* shared_out;            // gemm2 out: [T][d]
   bool out_bf16;
   int T, k, E, P, d, f, fs, fmax;
+  int routed_on, shared_on;    // which groups this launch computes (FfnPart)
   int TN;                      // token rows per tile; MMA N = TERMS * TN
   int stages, acc_bufs, tmem_cols, sf_col0;
   unsigned* status;
@@ -148,8 +149,12 @@ ffn_nvf4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     fence_barrier_init();
   }
   pdl_enter();   // from here on the kernel reads what earlier kernels wrote
-  if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kN4BM, a.fs / kN4BM, a.status);
-  else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kN4BM, a.d / kN4BM, a.status);
+  if (MODE == 1)
+    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN,
+                      a.routed_on ? a.f / kN4BM : 0, a.shared_on ? a.fs / kN4BM : 0, a.status);
+  else
+    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN,
+                      a.routed_on ? a.d / kN4BM : 0, a.shared_on ? a.d / kN4BM : 0, a.status);
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
     tmem_relinquish();
@@ -434,7 +439,8 @@ ffn_nvf4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
 // any rounding of the quotient, so a reciprocal product serves.
 // One CTA of kN4QThreads threads per row of the (P+T)-row activation space;
 // a thread holds 8 consecutive elements of every kN4QThreads*8-element chunk
-// (a 16-element block spans a thread pair).  GATHER_X: row r < P takes
+// (a 16-element block spans a thread pair); rows row_begin + blockIdx.x.
+// GATHER_X: row r < P takes
 // x[sorted_pair[r]/k], row P+t takes x[t] (width d); otherwise row r of H
 // (width f for routed rows, f_s for shared rows).  Outputs, row r term t at
 // row r*TERMS + t: packed codes (element 2i in the low nibble), block-scale
@@ -475,12 +481,13 @@ template <bool GATHER_X, int TERMS>
 __global__ void __launch_bounds__(kN4QThreads)
 nvf4_terms_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                   int width_r, int width_s, int src_stride, uint8_t* __restrict__ codes, int code_stride,
-                  uint8_t* __restrict__ scales, int scale_stride, float* __restrict__ gsc, unsigned* status) {
+                  uint8_t* __restrict__ scales, int scale_stride, float* __restrict__ gsc, int row_begin,
+                  unsigned* status) {
   pdl_enter();
   constexpr int kChunks = kN4MaxWidth / kN4QChunk;
   constexpr int kWarps = kN4QThreads / 32;
   __shared__ float red[TERMS][kWarps];
-  const int row = blockIdx.x;
+  const int row = row_begin + blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (row >= P + T) return;
   const uint16_t* s;
@@ -647,7 +654,7 @@ N4Plan n4_plan(const moe_config_t& c) {
 template <int MODE, int TERMS>
 cudaError_t launch_n4_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUtensorMap& mSA,
                            const CUtensorMap& mSAS, const CUtensorMap& mB, const CUtensorMap& mSB, N4Args a,
-                           int wtiles_max, int num_sms, cudaStream_t stream) {
+                           int wtiles_routed, int wtiles_shared, int grid_cap, cudaStream_t stream) {
   constexpr int NA = (MODE == 1) ? 2 : 1;
   const int N = TERMS * a.TN;
   if (N % 16 != 0 || N < 16 || N > 128) return cudaErrorInvalidConfiguration;
@@ -679,9 +686,9 @@ cudaError_t launch_n4_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const 
   cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_nvf4_kernel<MODE, TERMS>),
                                         static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  const long long tiles_ub =
-      static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
+  const long long tiles_ub = (a.routed_on ? static_cast<long long>(wtiles_routed) * (a.P / a.TN + a.E) : 0) +
+                             (a.shared_on ? static_cast<long long>(wtiles_shared) * ((a.T + a.TN - 1) / a.TN) : 0);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(grid_cap, tiles_ub)));
   count_launches(1);
   return launch_pdl(ffn_nvf4_kernel<MODE, TERMS>, grid, kN4Threads, smem, stream, mA, mAS, mSA, mSAS, mB, mSB, a);
 }
@@ -689,7 +696,7 @@ cudaError_t launch_n4_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const 
 template <int TERMS>
 cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                      const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out, void* ws,
-                     unsigned* status, int num_sms, cudaStream_t stream) {
+                     unsigned* status, int num_sms, const FfnPart& part, cudaStream_t stream) {
   const int T = c.T, k = c.top_k, E = c.n_experts, d = c.d_model, f = c.d_ff, fs = c.d_ff_shared;
   const int P = T * k, R = P + T;
   const int fmax = std::max(f, fs);
@@ -704,9 +711,12 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
   float* hg = reinterpret_cast<float*>(base + pl.hg);
   const uint64_t TR = static_cast<uint64_t>(R) * TERMS;
 
+  const int r0 = part.row_begin(P), r1 = part.row_end(P, T);
+  const int cap = std::min(num_sms, part.grid_cap);
   count_launches(1);
-  cudaError_t err = launch_pdl(nvf4_terms_kernel<true, TERMS>, R, kN4QThreads, 0, stream, static_cast<const uint16_t*>(x),
-                               sorted_pair, P, T, k, d, d, d, xq, d / 2, xs, d / 16, xg, status);
+  cudaError_t err = launch_pdl(nvf4_terms_kernel<true, TERMS>, r1 - r0, kN4QThreads, 0, stream,
+                               static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d, d, d, xq, d / 2, xs, d / 16,
+                               xg, r0, status);
   if (err != cudaSuccess) return err;
 
   N4Args a = {};
@@ -714,6 +724,7 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
   a.h = h; a.out_perm = out_perm; a.shared_out = shared_out;
   a.out_bf16 = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0;
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
+  a.routed_on = part.routed; a.shared_on = part.shared;
   a.TN = pl.TN; a.status = status;
 
   CUtensorMap mA, mAS, mSA, mSAS, mB, mSB;
@@ -727,12 +738,13 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
     return cudaErrorInvalidValue;
   a.wg = w->w13_gscale; a.sg = w->s13_gscale;
   a.b_scale = xg;
-  err = launch_n4_gemm<1, TERMS>(mA, mAS, mSA, mSAS, mB, mSB, a, fmax / kN4BM, num_sms, stream);
+  err = launch_n4_gemm<1, TERMS>(mA, mAS, mSA, mSAS, mB, mSB, a, f / kN4BM, fs / kN4BM, cap, stream);
   if (err != cudaSuccess) return err;
 
   count_launches(1);
-  err = launch_pdl(nvf4_terms_kernel<false, TERMS>, R, kN4QThreads, 0, stream, reinterpret_cast<const uint16_t*>(h),
-                   static_cast<const int32_t*>(nullptr), P, T, k, f, fs, fmax, hq, fmax / 2, hs, fmax / 16, hg, status);
+  err = launch_pdl(nvf4_terms_kernel<false, TERMS>, r1 - r0, kN4QThreads, 0, stream,
+                   reinterpret_cast<const uint16_t*>(h), static_cast<const int32_t*>(nullptr), P, T, k, f, fs, fmax, hq,
+                   fmax / 2, hs, fmax / 16, hg, r0, status);
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs
@@ -745,7 +757,7 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
     return cudaErrorInvalidValue;
   a.wg = w->w2_gscale; a.sg = w->s2_gscale;
   a.b_scale = hg;
-  return launch_n4_gemm<2, TERMS>(mA, mAS, mSA, mSAS, mB, mSB, a, d / kN4BM, num_sms, stream);
+  return launch_n4_gemm<2, TERMS>(mA, mAS, mSA, mSAS, mB, mSB, a, d / kN4BM, d / kN4BM, cap, stream);
 }
 
 }  // namespace
@@ -772,11 +784,11 @@ size_t ffn_nvf4_ws_bytes(const moe_config_t& c) { return n4_plan(c).total; }
 
 cudaError_t launch_ffn_nvf4(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                             const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
-                            void* ws, unsigned* status, int num_sms, cudaStream_t stream) {
+                            void* ws, unsigned* status, int num_sms, const FfnPart& part, cudaStream_t stream) {
   if (c.T == 0) return cudaSuccess;
   if (c.flags & MOE_FLAG_ACT_NVFP4)
-    return run_nvf4<1>(c, x, topk_w, offsets, sorted_pair, w, out_perm, shared_out, ws, status, num_sms, stream);
-  return run_nvf4<4>(c, x, topk_w, offsets, sorted_pair, w, out_perm, shared_out, ws, status, num_sms, stream);
+    return run_nvf4<1>(c, x, topk_w, offsets, sorted_pair, w, out_perm, shared_out, ws, status, num_sms, part, stream);
+  return run_nvf4<4>(c, x, topk_w, offsets, sorted_pair, w, out_perm, shared_out, ws, status, num_sms, part, stream);
 }
 
 }  // namespace moe

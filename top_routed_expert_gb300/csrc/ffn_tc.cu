@@ -73,6 +73,7 @@ struct TcArgs {
   void* shared_out;            // gemm2 out: [T][d]
   bool out_bf16;
   int T, k, E, P, d, f, fs, fmax;
+  int routed_on, shared_on;    // which groups this launch computes (FfnPart)
   int TN;                      // token rows per tile; MMA N = TERMS*TN
   int stages, acc_bufs, tmem_cols;
   uint64_t wait_ns;            // limit of every bounded wait
@@ -128,8 +129,12 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   // kernel reads what earlier kernels wrote
   pdl_enter();
   // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
-  if (MODE == 1) build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.f / kBM, a.fs / kBM, a.status);
-  else build_group_table(c->gt, a.offsets, a.E, a.P, a.T, a.TN, a.d / kBM, a.d / kBM, a.status);
+  if (MODE == 1)
+    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN, a.routed_on ? a.f / kBM : 0,
+                      a.shared_on ? a.fs / kBM : 0, a.status);
+  else
+    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN, a.routed_on ? a.d / kBM : 0,
+                      a.shared_on ? a.d / kBM : 0, a.status);
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
     tmem_relinquish();
@@ -361,18 +366,19 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
 // amax <= 448 s (1 for an all-zero row), hi and lo E4M3 (round to nearest
 // even, saturating).  With two_terms false only hi is written: the single-
 // term 8-bit activation of MOE_FLAG_ACT_E4M3.  One warp per row of the
-// (P+T)-row activation space.  GATHER_X: row r < P takes x[sorted_pair[r]/k],
-// row P+t takes x[t] (width d); otherwise row r of H (width f for routed
-// rows, f_s for shared rows).  Output q[2r] = hi codes, q[2r+1] = lo codes.
+// (P+T)-row activation space, rows [row_begin, row_end).  GATHER_X: row
+// r < P takes x[sorted_pair[r]/k], row P+t takes x[t] (width d); otherwise
+// row r of H (width f for routed rows, f_s for shared rows).  Output
+// q[2r] = hi codes, q[2r+1] = lo codes.
 template <bool GATHER_X, bool IN_REGS>
 __global__ void __launch_bounds__(256)
 quant2_rows_kernel(const uint16_t* __restrict__ src, const int32_t* __restrict__ sorted_pair, int P, int T, int k,
                    int width_r, int width_s, int src_stride, uint8_t* __restrict__ q, int q_stride,
-                   float* __restrict__ scale, bool two_terms, unsigned* status) {
+                   float* __restrict__ scale, bool two_terms, int row_begin, int row_end, unsigned* status) {
   pdl_enter();
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int row = row_begin + blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= P + T) return;
+  if (row >= row_end) return;
   const uint16_t* s;
   int width;
   uint8_t* qh = q + static_cast<size_t>(2 * row) * q_stride;
@@ -535,7 +541,7 @@ TcPlan plan(const moe_config_t& c) {
 
 template <int MODE, int TERMS>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUtensorMap& mB, TcArgs a,
-                        int wtiles_max, int num_sms, cudaStream_t stream) {
+                        int wtiles_routed, int wtiles_shared, int grid_cap, cudaStream_t stream) {
   constexpr int NA = (MODE == 1) ? 2 : 1;
   const int N = TERMS * a.TN;
   const int stage_bytes = NA * kABytes + align_up(static_cast<size_t>(N) * kBK, 1024);
@@ -556,9 +562,9 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUt
   cudaError_t err =
       ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_tc_kernel<MODE, TERMS>), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  const long long tiles_ub =
-      static_cast<long long>(wtiles_max) * (a.P / a.TN + a.E + (a.T + a.TN - 1) / a.TN + 1);
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, tiles_ub)));
+  const long long tiles_ub = (a.routed_on ? static_cast<long long>(wtiles_routed) * (a.P / a.TN + a.E) : 0) +
+                             (a.shared_on ? static_cast<long long>(wtiles_shared) * ((a.T + a.TN - 1) / a.TN) : 0);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(grid_cap, tiles_ub)));
   count_launches(1);
   return launch_pdl(ffn_tc_kernel<MODE, TERMS>, grid, kTcThreads, smem, stream, mA, mAS, mB, a);
 }
@@ -574,7 +580,7 @@ size_t ffn_tc_ws_bytes(const moe_config_t& c) { return plan(c).total; }
 
 cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* topk_w, const int32_t* offsets,
                           const int32_t* sorted_pair, const moe_weights_t* w, void* out_perm, void* shared_out,
-                          void* ws, unsigned* status, int num_sms, cudaStream_t stream) {
+                          void* ws, unsigned* status, int num_sms, const FfnPart& part, cudaStream_t stream) {
   const int T = c.T, k = c.top_k, E = c.n_experts, d = c.d_model, f = c.d_ff, fs = c.d_ff_shared;
   if (T == 0) return cudaSuccess;
   const int P = T * k, R = P + T;
@@ -598,12 +604,14 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
 
   // few rows (decode): keep each row in registers (one read, all loads in
   // flight); many rows: a lean two-pass kernel keeps more warps resident
-  const int qblocks = ceil_div(R, 8);
+  const int r0 = part.row_begin(P), r1 = part.row_end(P, T);
+  const int qblocks = ceil_div(r1 - r0, 8);
   const bool regs = R <= 4096;
+  const int cap = std::min(num_sms, part.grid_cap);
   count_launches(1);
   cudaError_t err = launch_pdl(regs ? quant2_rows_kernel<true, true> : quant2_rows_kernel<true, false>, qblocks, 256, 0,
                                stream, static_cast<const uint16_t*>(x), sorted_pair, P, T, k, d, d, d, xq, d, sx,
-                               !one_term, status);
+                               !one_term, r0, r1, status);
   if (err != cudaSuccess) return err;
 
   CUtensorMap mA, mAS, mB;
@@ -612,6 +620,7 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   a.h = h; a.out_perm = out_perm; a.shared_out = shared_out;
   a.out_bf16 = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0;
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
+  a.routed_on = part.routed; a.shared_on = part.shared;
   a.TN = pl.TN; a.status = status;
   const bool inject = (c.flags & MOE_FLAG_INJECT_TIMEOUT) != 0;
   a.wait_ns = inject ? 20000000ull : kWaitLimitNs;
@@ -627,14 +636,14 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   a.as_scale = static_cast<const float*>(w->s13_scale);
   a.b_scale = sx;
   a.TN = tn1;   // two buffers of (gate, up) x TERMS*TN columns fit TMEM at TERMS*TN <= 128
-  err = one_term ? launch_gemm<1, 1>(mA, mAS, mB, a, std::max(f, fs) / kBM, num_sms, stream)
-                 : launch_gemm<1, 2>(mA, mAS, mB, a, std::max(f, fs) / kBM, num_sms, stream);
+  err = one_term ? launch_gemm<1, 1>(mA, mAS, mB, a, f / kBM, fs / kBM, cap, stream)
+                 : launch_gemm<1, 2>(mA, mAS, mB, a, f / kBM, fs / kBM, cap, stream);
   if (err != cudaSuccess) return err;
 
   count_launches(1);
   err = launch_pdl(regs ? quant2_rows_kernel<false, true> : quant2_rows_kernel<false, false>, qblocks, 256, 0, stream,
                    reinterpret_cast<const uint16_t*>(h), static_cast<const int32_t*>(nullptr), P, T, k, f, fs, fmax,
-                   hq, fmax, sh, !one_term, status);
+                   hq, fmax, sh, !one_term, r0, r1, status);
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs
@@ -648,8 +657,8 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   a.as_scale = static_cast<const float*>(w->s2_scale);
   a.b_scale = sh;
   a.TN = tn2;
-  return one_term ? launch_gemm<2, 1>(mA, mAS, mB, a, d / kBM, num_sms, stream)
-                  : launch_gemm<2, 2>(mA, mAS, mB, a, d / kBM, num_sms, stream);
+  return one_term ? launch_gemm<2, 1>(mA, mAS, mB, a, d / kBM, d / kBM, cap, stream)
+                  : launch_gemm<2, 2>(mA, mAS, mB, a, d / kBM, d / kBM, cap, stream);
 }
 
 }  // namespace moe

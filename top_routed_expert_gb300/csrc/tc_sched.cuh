@@ -35,10 +35,13 @@ __device__ __forceinline__ Tile decode_tile(const GroupTable& gt, int G, int i, 
 
 
 // Fills the table for E routed groups plus the shared group; wtiles_routed /
-// wtiles_shared weight tiles per group, token tiles of TN rows.  Offsets that
-// are not monotone or leave [0, P] make that group empty and record
-// MOE_ERR_DEVICE_BOUNDS.  Called by every thread of the block (it contains
-// __syncthreads): one thread per group fills the group's entries, then warp 0
+// wtiles_shared weight tiles per group (0 leaves that part out), token tiles
+// of TN rows.  Offsets that are not monotone or leave [0, P] make that group
+// empty and record MOE_ERR_DEVICE_BOUNDS; offsets == nullptr (a launch of the
+// shared part alone, which may run while the offsets are being written)
+// makes every routed group empty without reading them.  Called by every
+// thread of the block (it contains __syncthreads): one thread per group
+// fills the group's entries, then warp 0
 // turns the per-group tile counts into their exclusive prefix sum with warp
 // shuffles.  Returns after the table is visible to the whole block.
 __device__ __forceinline__ void build_group_table(GroupTable& gt, const int32_t* offsets, int E, int P, int T, int TN,
@@ -46,7 +49,10 @@ __device__ __forceinline__ void build_group_table(GroupTable& gt, const int32_t*
   const int G = E + 1;
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     int base, rows;
-    if (g < E) {
+    if (g < E && offsets == nullptr) {
+      base = 0;
+      rows = 0;
+    } else if (g < E) {
       base = offsets[g];
       rows = offsets[g + 1] - base;
       if (base < 0 || rows < 0 || base + rows > P) {
