@@ -101,10 +101,10 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_NVFP4 = 3 } moe_dtyp
  * exactly in f16 in shared memory, kind::f16 MMAs); the path that also
  * serves NVFP4 widths the block-scaled path does not take. */
 #define MOE_FLAG_NVFP4_F16 0x20u
-/* moe_layer_forward runs the shared expert on a second stream beside the
- * routing by default (see moe_layer_forward); with this flag it runs in the
- * same launches as the routed experts, after the routing, on `stream` only.
- * The results are the same bit for bit. */
+/* moe_layer_forward runs the shared expert of a decode-sized batch on a
+ * second stream beside the routing by default (see moe_layer_forward); with
+ * this flag it runs in the same launches as the routed experts, after the
+ * routing, on `stream` only.  The results are the same bit for bit. */
 #define MOE_FLAG_NO_OVERLAP 0x40u
 /* Test hook for the failure path: in the tensor-core expert GEMM, CTA 0
  * withholds one "accumulator ready" signal and every bounded wait shortens to
@@ -276,13 +276,15 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* out_perm, const in
 
 /*
  * The whole layer: route -> permute -> expert FFN (+ shared) -> combine, with
- * no host synchronisation.  The shared expert needs no routing result, so it
+ * no host synchronisation.  The shared expert needs no routing result, so
+ * for decode-sized batches (at most 16 routed rows per expert on average) it
  * runs beside the routing (Sarvam blog, Table 1 row "Shared expert compute"
  * and the paragraph on hiding latency by overlap): the call forks a stream
  * of the library's own (created with the device's first call) off `stream`,
- * runs the shared expert there on its share of the SMs, runs route ->
- * permute -> routed experts on `stream`, and makes `stream` wait for the
- * fork before the combine.  To the caller this is one call on `stream`: the
+ * runs the shared expert there on at most half the SMs while the routing
+ * runs on `stream`, then the routed experts on `stream`, and makes `stream`
+ * wait for the fork before the combine.  Larger batches keep the shared
+ * expert in the routed launches.  To the caller this is one call on `stream`: the
  * results are ready when `stream` reaches them, and the call records into a
  * CUDA graph captured on `stream` as a fork and a join.  Calls on one device
  * share that second stream, so their shared-expert parts run one after

@@ -751,11 +751,14 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   a.out_bf16 = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0;
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
   a.routed_on = part.routed; a.shared_on = part.shared;
-  a.TN = pl.TN; a.status = status;
+  // token tile: from the average routed group, or, for the shared expert
+  // alone, from T
+  a.TN = part.routed ? pl.TN : (T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128);
+  a.status = status;
 
   CUtensorMap mB, mA, mAs;
   // gemm1: gate / up
-  if (!make_f16_map(&mB, xh, R, d, d, pl.TN) ||
+  if (!make_f16_map(&mB, xh, R, d, d, a.TN) ||
       !make_code_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d) ||
       !make_code_map(&mAs, w->s13, 2 * static_cast<uint64_t>(fs), d))
     return cudaErrorInvalidValue;
@@ -772,7 +775,7 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs
-  if (!make_f16_map(&mB, hh, R, fmax, fmax, pl.TN) ||
+  if (!make_f16_map(&mB, hh, R, fmax, fmax, a.TN) ||
       !make_code_map(&mA, w->w2, static_cast<uint64_t>(E) * d, f) ||
       !make_code_map(&mAs, w->s2, static_cast<uint64_t>(d), fs))
     return cudaErrorInvalidValue;

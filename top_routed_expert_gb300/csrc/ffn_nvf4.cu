@@ -725,7 +725,12 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
   a.out_bf16 = (c.flags & MOE_FLAG_BF16_EXPERT_OUT) != 0;
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
   a.routed_on = part.routed; a.shared_on = part.shared;
-  a.TN = pl.TN; a.status = status;
+  // token tile: from the average routed group, or, for the shared expert
+  // alone, from T (N = TERMS * TN <= 128)
+  const int tn_cap = 128 / TERMS;
+  const int tn_sh = T <= 4 ? 4 : T <= 8 ? 8 : T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128;
+  a.TN = part.routed ? pl.TN : std::max(16 / TERMS, std::min(tn_sh, tn_cap));
+  a.status = status;
 
   CUtensorMap mA, mAS, mSA, mSAS, mB, mSB;
   // gemm1: gate / up
@@ -733,8 +738,8 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
       !make_byte_map(&mAS, w->s13, static_cast<uint64_t>(2) * fs, d / 2, kN4BK, kN4BM) ||
       !make_byte_map(&mSA, w->w13_scale, static_cast<uint64_t>(E) * 2 * f, d / 16, 16, kN4BM) ||
       !make_byte_map(&mSAS, w->s13_scale, static_cast<uint64_t>(2) * fs, d / 16, 16, kN4BM) ||
-      !make_byte_map(&mB, xq, TR, d / 2, kN4BK, TERMS * pl.TN) ||
-      !make_byte_map(&mSB, xs, TR, d / 16, 16, TERMS * pl.TN))
+      !make_byte_map(&mB, xq, TR, d / 2, kN4BK, TERMS * a.TN) ||
+      !make_byte_map(&mSB, xs, TR, d / 16, 16, TERMS * a.TN))
     return cudaErrorInvalidValue;
   a.wg = w->w13_gscale; a.sg = w->s13_gscale;
   a.b_scale = xg;
@@ -752,8 +757,8 @@ cudaError_t run_nvf4(const moe_config_t& c, const void* x, const float* topk_w, 
       !make_byte_map(&mAS, w->s2, static_cast<uint64_t>(d), fs / 2, kN4BK, kN4BM) ||
       !make_byte_map(&mSA, w->w2_scale, static_cast<uint64_t>(E) * d, f / 16, 16, kN4BM) ||
       !make_byte_map(&mSAS, w->s2_scale, static_cast<uint64_t>(d), fs / 16, 16, kN4BM) ||
-      !make_byte_map(&mB, hq, TR, fmax / 2, kN4BK, TERMS * pl.TN) ||
-      !make_byte_map(&mSB, hs, TR, fmax / 16, 16, TERMS * pl.TN))
+      !make_byte_map(&mB, hq, TR, fmax / 2, kN4BK, TERMS * a.TN) ||
+      !make_byte_map(&mSB, hs, TR, fmax / 16, 16, TERMS * a.TN))
     return cudaErrorInvalidValue;
   a.wg = w->w2_gscale; a.sg = w->s2_gscale;
   a.b_scale = hg;

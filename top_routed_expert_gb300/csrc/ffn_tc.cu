@@ -589,12 +589,16 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   // activation terms per row: 2 (exact), or 1 with MOE_FLAG_ACT_E4M3 (the
   // MMA's N is then the token count, at least 16)
   const bool one_term = (c.flags & MOE_FLAG_ACT_E4M3) != 0;
-  const int tn1 = one_term ? std::max(16, std::min(pl.TN, 128)) : std::min(pl.TN, MOE_TC_TN1_CAP);
+  // token tile: from the average routed group, or, for the shared expert
+  // alone, from T (one group of T rows: the fewest tiles, so each weight tile
+  // is read as few times as possible)
+  const int tn = part.routed ? pl.TN : (T <= 8 ? 8 : T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128);
+  const int tn1 = one_term ? std::max(16, std::min(tn, 128)) : std::min(tn, MOE_TC_TN1_CAP);
   // one term, down GEMM: 256-token tiles once groups are that large (N = 256
   // halves the operand bytes per MAC of a 128 x 128 tile; K = f is short, so
   // the feed, not the MMA, bounds the smaller tile)
-  const int tn2 = one_term ? (static_cast<double>(P) / E > 96 ? 256 : std::max(16, std::min(pl.TN, 128)))
-                           : std::min(pl.TN, MOE_TC_TN2_CAP);
+  const bool big = part.routed ? static_cast<double>(P) / E > 96 : T > 96;
+  const int tn2 = one_term ? (big ? 256 : std::max(16, std::min(tn, 128))) : std::min(tn, MOE_TC_TN2_CAP);
   char* base = static_cast<char*>(ws);
   uint8_t* xq = reinterpret_cast<uint8_t*>(base + pl.xq);
   float* sx = reinterpret_cast<float*>(base + pl.sx);
