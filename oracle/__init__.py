@@ -10,3 +10,4 @@ from .moe_oracle import (E2M1_TABLE, E4M3_TABLE, decode_bf16, decode_e2m1_packed
                          shared_weights, silu, swiglu_ffn, topk_ids, x_values,
                          encode_e4m3, act_scale, quantize_act_rows, round_bf16,
                          encode_e2m1, nvfp4_row_scale, nvfp4_block_scale, quantize_nvfp4_act_rows)
+from . import qk_rope_oracle  # noqa: F401,E402
