@@ -467,6 +467,54 @@ def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_ter
     return roof, t_layer_roof / (ms_step / 1e3)
 
 
+def qk_rope_point(args, world, dev, gpu_index, abi, torch):
+    """moe_qk_norm_rope on the T = 8192 prefill batch (32 query / 4 key heads
+    of 128).  q and k (75 MB) fit in L2, so a 512 MB buffer is written
+    between launches and each launch is timed alone with CUDA events on the
+    launching stream; the roofline is HBM: q and k read and written once,
+    plus the table rows, positions and gammas."""
+    import moe_synth
+    from top_routed_expert_gb300.layer import _to_dev
+    inp = moe_synth.make_qk_inputs()
+    q, k = _to_dev(inp.q, dev).clone(), _to_dev(inp.k, dev).clone()
+    gq, gk = _to_dev(inp.gamma_q, dev), _to_dev(inp.gamma_k, dev)
+    cs, pos = _to_dev(inp.cos_sin, dev), _to_dev(inp.positions, dev)
+    cfg = abi.moe_qk_rope_config_t(inp.T, inp.n_q_heads, inp.n_kv_heads, inp.head_dim, inp.n_pos, 1e-6)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(5, args.steps)
+    for _ in range(args.warmup):
+        abi.moe_qk_norm_rope(cfg, q, k, gq, gk, cs, pos, stream)
+    if abi.moe_get_device_status(stream) != 0:
+        raise RuntimeError("moe_qk_norm_rope reported a device fault")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(gpu_index) as clk:
+        torch.cuda.synchronize(dev)
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            abi.moe_qk_norm_rope(cfg, q, k, gq, gk, cs, pos, stream)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+    us = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps, world, dev) * 1e3
+    rows = inp.T * (inp.n_q_heads + inp.n_kv_heads)
+    n_used = len(np.unique(inp.positions))
+    bytes_ = 2 * rows * inp.head_dim * 2 + n_used * inp.head_dim // 2 * 8 + 4 * inp.T + 2 * 4 * inp.head_dim
+    peaks, src = load_peaks()
+    achieved = bytes_ / (us * 1e-6) / 1e9
+    return {"workload": f"fused QK-norm + RoPE, in place: T={inp.T}, {inp.n_q_heads} query / {inp.n_kv_heads} key heads "
+                        f"of {inp.head_dim}, bf16, rotate-half RoPE from a {inp.n_pos}-row float32 table",
+            "value": job_value(world, inp.T, us / 1e3), "unit": "tokens/s", "us_per_launch": us, "steps": steps,
+            "l2": "512 MB written between launches (q and k, 75 MB, would otherwise stay in L2); each launch timed "
+                  "alone",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "qk_norm_rope_kernel", "peak_source": f"{src}: HBM copy GB/s",
+                         "algorithmic_bytes": bytes_},
+            "pages_context": "Sarvam blog Table 1: 414 -> 54 us per layer on H100 (their batch size not given)",
+            "clocks": clk.summary()}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import moe_synth
@@ -601,6 +649,10 @@ def run_ours(args, world, rank, local):
                 del lf, lw
             del l100, inp100
             torch.cuda.empty_cache()
+
+    # the fused QK-norm + RoPE step of the same model's attention block
+    if args.workload == "decode" and not args.no_prefill:
+        points["qk_norm_rope"] = qk_rope_point(args, world, dev, gpu_index, abi, torch)
 
     if rank != 0:
         return

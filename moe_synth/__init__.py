@@ -38,7 +38,8 @@ from typing import Optional
 import numpy as np
 import torch
 
-__all__ = ["CONFIGS", "MoEInputs", "make_inputs", "make_custom", "with_heavy_tails", "bf16_bits_to_f32",
+__all__ = ["CONFIGS", "MoEInputs", "make_inputs", "make_custom", "with_heavy_tails", "QKInputs", "make_qk_inputs",
+           "bf16_bits_to_f32",
            "quantize_e4m3_rows", "quantize_nvfp4", "SKEW_C", "SKEW_DEAD"]
 
 
@@ -265,3 +266,53 @@ def with_heavy_tails(inp: MoEInputs, per_row: int = 3, magnitude: float = 1000.0
         xf[t, cols] = np.float32(magnitude) * rng.choice(np.array([-1.0, 1.0], dtype=np.float32), size=per_row)
     x = _f32_to_bf16_bits(xf) if inp.cfg.x_dtype == "bf16" else xf
     return dataclasses.replace(inp, x=x)
+
+
+# ---------------------------------------------------------------------------
+# Inputs of the fused QK-norm + RoPE step (attention block of the same
+# model: d_model 4096 = 32 query heads of width 128, grouped-query attention
+# with 4 key heads).  A prefill batch of 32 requests x 256-token chunks, each
+# request's chunk at a seeded offset inside a 3584-token prompt (the pages'
+# input sequence length); the frequency table covers 4096 positions.
+
+
+@dataclasses.dataclass
+class QKInputs:
+    T: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    q: np.ndarray           # [T][Hq][D] uint16 bf16 bits
+    k: np.ndarray           # [T][Hkv][D] uint16 bf16 bits
+    gamma_q: np.ndarray     # [D] float32
+    gamma_k: np.ndarray     # [D] float32
+    cos_sin: np.ndarray     # [n_pos][D/2][2] float32
+    positions: np.ndarray   # [T] int32
+
+    @property
+    def n_pos(self) -> int:
+        return self.cos_sin.shape[0]
+
+
+def make_qk_inputs(T=8192, n_q_heads=32, n_kv_heads=4, head_dim=128, n_pos=4096, chunk=256, prompt=3584,
+                   theta=10000.0, seed=0) -> QKInputs:
+    """q, k ~ N(0,1) with a seeded log-normal scale per (token, head) row
+    (so the normalisation has something to do), gammas ~ U(0.5, 1.5), the
+    (cos, sin) table of pos * theta^(-2i/D) rounded to float32, positions of
+    consecutive chunks at seeded offsets."""
+    ss = np.random.SeedSequence(seed).spawn(6)
+    rq, rk, rg, rp = (np.random.default_rng(x) for x in ss[:4])
+    qf = rq.standard_normal((T, n_q_heads, head_dim), dtype=np.float32)
+    qf *= np.exp(rq.standard_normal((T, n_q_heads, 1))).astype(np.float32)
+    kf = rk.standard_normal((T, n_kv_heads, head_dim), dtype=np.float32)
+    kf *= np.exp(rk.standard_normal((T, n_kv_heads, 1))).astype(np.float32)
+    gq = rg.uniform(0.5, 1.5, head_dim).astype(np.float32)
+    gk = rg.uniform(0.5, 1.5, head_dim).astype(np.float32)
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    ang = np.arange(n_pos, dtype=np.float64)[:, None] * theta ** (-2.0 * i / head_dim)[None, :]
+    cs = np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+    n_req = (T + chunk - 1) // chunk
+    offs = rp.integers(0, max(1, min(prompt, n_pos) - chunk + 1), n_req)
+    t = np.arange(T)
+    pos = (offs[t // chunk] + t % chunk).astype(np.int32)
+    return QKInputs(T, n_q_heads, n_kv_heads, head_dim, _f32_to_bf16_bits(qf), _f32_to_bf16_bits(kf), gq, gk, cs, pos)

@@ -174,3 +174,19 @@ def test_act_nvfp4_flag_validation(lib):
                 dict(flags=abi.MOE_FLAG_ACT_NVFP4 | abi.MOE_FLAG_SIMT_FFN, **nv),
                 dict(flags=abi.MOE_FLAG_ACT_NVFP4, x_dtype=abi.MOE_F32, **nv)):
         assert lib.moe_workspace_bytes(ctypes.byref(cfg(**bad))) == 0, bad
+
+
+def test_qk_norm_rope_rejects_bad_arguments(lib):
+    fake = ctypes.c_void_p(0x10000)
+    good = dict(T=4, n_q_heads=2, n_kv_heads=1, head_dim=128, n_pos=8, eps=1e-6)
+    for bad in (dict(head_dim=96), dict(head_dim=0), dict(T=-1), dict(n_kv_heads=0), dict(n_pos=0),
+                dict(eps=0.0), dict(eps=float("nan"))):
+        c = abi.moe_qk_rope_config_t(**dict(good, **bad))
+        assert lib.moe_qk_norm_rope(ctypes.byref(c), fake, fake, fake, fake, fake, fake, None) == 1, bad
+    c = abi.moe_qk_rope_config_t(**good)
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.moe_qk_norm_rope(ctypes.byref(c), odd, fake, fake, fake, fake, fake, None) == 1   # misaligned
+    assert lib.moe_qk_norm_rope(ctypes.byref(c), None, fake, fake, fake, fake, fake, None) == 1
+    assert lib.moe_qk_norm_rope(None, fake, fake, fake, fake, fake, fake, None) == 1
+    c0 = abi.moe_qk_rope_config_t(**dict(good, T=0))
+    assert lib.moe_qk_norm_rope(ctypes.byref(c0), None, None, None, None, None, None, None) == 0

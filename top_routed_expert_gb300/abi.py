@@ -35,7 +35,8 @@ STATUS = {
 
 # Every symbol include/moe_gb300.h declares.
 EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_route", "moe_permute",
-           "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_launch_count", "moe_get_device_status")
+           "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_launch_count",
+           "moe_get_device_status", "moe_qk_norm_rope")
 
 
 class MoEError(RuntimeError):
@@ -49,6 +50,11 @@ class moe_config_t(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32),
                 ("x_dtype", ctypes.c_int32), ("w_dtype", ctypes.c_int32), ("y_dtype", ctypes.c_int32),
                 ("flags", ctypes.c_uint32)]
+
+
+class moe_qk_rope_config_t(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_pos", ctypes.c_int32), ("eps", ctypes.c_float)]
 
 
 class moe_weights_t(ctypes.Structure):
@@ -83,6 +89,7 @@ def load(path: str = LIB) -> ctypes.CDLL:
         "moe_layer_forward": (i32, [cfgp, vp, vp, vp, wp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_launch_count": (ctypes.c_uint64, []),
         "moe_get_device_status": (i32, [vp]),
+        "moe_qk_norm_rope": (i32, [ctypes.POINTER(moe_qk_rope_config_t), vp, vp, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -173,6 +180,12 @@ def moe_layer_forward(cfg, x, w_router, expert_bias, weights: moe_weights_t, y, 
                                     _ptr(expert_offsets), _ptr(ws),
                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
            "moe_layer_forward")
+
+
+def moe_qk_norm_rope(cfg, q, k, gamma_q, gamma_k, cos_sin, positions, stream=None):
+    """Fused QK-norm + RoPE, in place on q [T, Hq, D] and k [T, Hkv, D] (bf16)."""
+    _check(load().moe_qk_norm_rope(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(gamma_q), _ptr(gamma_k),
+                                   _ptr(cos_sin), _ptr(positions), _stream(stream)), "moe_qk_norm_rope")
 
 
 def moe_launch_count() -> int:
