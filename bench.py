@@ -413,6 +413,18 @@ def time_graph(layer, x, steps, warmup, world, dev, torch, gpu_index=None):
 TENSOR_WORKLOADS = ("prefill", "100b_prefill")
 
 
+def nvfp4_on_f16_path(cfg, flags):
+    """Whether the library runs these NVFP4 weights on the f16-rebuild path:
+    when forced, or for the exact contract at more than 16 routed rows per
+    expert on average (the block-scaled path takes decode-sized batches and
+    every batch with NVFP4 activations)."""
+    if flags & 0x20:          # MOE_FLAG_NVFP4_F16
+        return True
+    if flags & 0x10:          # MOE_FLAG_ACT_NVFP4
+        return False
+    return cfg.T * cfg.k > 16 * cfg.E
+
+
 def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_terms=None, nvfp4_f16=False):
     """Roofline of the dominant stage (moe_expert_ffn) and of the whole layer.
 
@@ -594,8 +606,9 @@ def run_ours(args, world, rank, local):
                 l1 = copy.copy(lay)
                 l1.flags = lay.flags | abi.MOE_FLAG_NO_OVERLAP
                 g1, _ = time_graph(l1, xp, steps, args.warmup, world, dev, torch, None)
+            f16 = nvfp4_f16 or (src.cfg.w_dtype == "nvfp4" and nvfp4_on_f16_path(src.cfg, lay.flags))
             rp, lfp = roofline(mp["alg"], mp["stage_ms"]["expert_ffn"], gp, name, src.cfg.w_dtype, args.simt,
-                               act_terms, nvfp4_f16)
+                               act_terms, f16)
             out = {"workload": WORKLOAD_TEXT[name], "value": job_value(world, src.cfg.T, gp), "unit": "tokens/s",
                    "ms_per_step": gp, "steps": steps, "roofline": rp, "layer_roofline_frac": lfp,
                    "active_experts": mp["alg"]["active"],
@@ -658,7 +671,8 @@ def run_ours(args, world, rank, local):
         return
     value = job_value(world, T, graph_ms)
     roof, layer_frac = roofline(m["alg"], m["stage_ms"]["expert_ffn"], graph_ms, args.workload, cfg.w_dtype,
-                                args.simt, 1 if args.act_e4m3 else None)
+                                args.simt, 1 if args.act_e4m3 else None,
+                                cfg.w_dtype == "nvfp4" and nvfp4_on_f16_path(cfg, flags))
     cpu = None
     if not args.no_cpu_baseline and world == 1:   # the oracle baseline: rank 0 of a single-GPU run only
         v, n, el = time_oracle(inp, args.cpu_budget)
@@ -670,7 +684,9 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": graph_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32" if args.simt else (
-            "e2m1 block-scaled MMA with fp32 accumulate (NVFP4 weights; four NVFP4 terms per activation row, bf16 H)"
+            ("f16 MMA with fp32 accumulate (NVFP4 weights rebuilt exactly in f16, row-scaled f16 activations, bf16 H)"
+             if nvfp4_on_f16_path(cfg, flags) else
+             "e2m1 block-scaled MMA with fp32 accumulate (NVFP4 weights; four NVFP4 terms per activation row, bf16 H)")
             if cfg.w_dtype == "nvfp4" else
             "e4m3 MMA with fp32 accumulate (one-term E4M3 activations: MOE_FLAG_ACT_E4M3, lossy)" if args.act_e4m3 else
             "e4m3 MMA with fp32 accumulate (two-term E4M3 activations, bf16 H)"),

@@ -79,3 +79,11 @@ def test_skew_reports_the_slower_bound():
     assert roof["bound"] == "hbm"
     roof, _ = bench.roofline(alg(0.5e9, 2.0e12), 0.6, 0.7, "skew", "e4m3")
     assert roof["bound"] == "tensor"
+
+
+def test_nvfp4_path_choice_follows_the_library():
+    from types import SimpleNamespace as NS
+    dec = NS(T=64, k=8, E=128)
+    pre = NS(T=8192, k=8, E=128)
+    assert not bench.nvfp4_on_f16_path(dec, 0) and bench.nvfp4_on_f16_path(pre, 0)
+    assert bench.nvfp4_on_f16_path(dec, 0x20) and not bench.nvfp4_on_f16_path(pre, 0x10)
