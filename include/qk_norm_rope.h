@@ -30,7 +30,8 @@ extern "C" {
 typedef struct {
   int32_t T;            /* tokens, >= 0 (0 is a no-op)                          */
   int32_t n_q_heads;    /* query heads, >= 1                                    */
-  int32_t n_kv_heads;   /* key heads, >= 1 (grouped-query attention: fewer)     */
+  int32_t n_kv_heads;   /* key heads, >= 1 (grouped-query attention: fewer);
+                           (n_q_heads + n_kv_heads) * head_dim * 2 <= 200 KB     */
   int32_t head_dim;     /* D: 64, 128 or 256                                    */
   int32_t n_pos;        /* rows of the frequency table, >= 1                    */
   float eps;            /* RMSNorm epsilon, > 0 and finite                      */
