@@ -553,7 +553,8 @@ def qk_rope_point(args, world, dev, gpu_index, abi, torch):
             "value": job_value(world, inp.T, us / 1e3), "unit": "tokens/s", "us_per_launch": us, "steps": steps,
             "l2": "512 MB read between launches (q and k, 75 MB, would otherwise stay in L2); each launch timed alone",
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("qk_norm_rope", "qk_norm_rope_kernel"),
                          "kernel": "qk_norm_rope_kernel", "peak_source": f"{src}: HBM copy GB/s",
                          "algorithmic_bytes": bytes_},
             "pages_context": "Sarvam blog Table 1: 414 -> 54 us per layer on H100 (their batch size not given)",
