@@ -47,7 +47,6 @@ constexpr int kMaxStages = 8;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: no legitimate wait comes close
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
 constexpr uint32_t kABytes = kBM * kBK;            // 16 KB per weight tile
-constexpr int kSmemBudget = 220 * 1024;
 
 // Tuning knobs (compile-time): largest token tile of the gate/up and of the
 // down GEMM, and the L2 promotion of the TMA loads.
@@ -545,7 +544,8 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUt
   constexpr int NA = (MODE == 1) ? 2 : 1;
   const int N = TERMS * a.TN;
   const int stage_bytes = NA * kABytes + align_up(static_cast<size_t>(N) * kBK, 1024);
-  a.stages = std::min(kMaxStages, kSmemBudget / stage_bytes);
+  // as many stages as fit next to the control block in 227 KB
+  a.stages = std::min(kMaxStages, static_cast<int>((227 * 1024 - 1024 - sizeof(TcCtrl)) / stage_bytes));
   const int per_acc = NA * N;
   a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
   // The epilogue reads 32 columns per load (gemm1: gate and up from column c0
