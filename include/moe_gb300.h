@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2   /* 2: NVFP4 block-scaled path and flags, shared-expert overlap, moe_qk_norm_rope */
 
 typedef enum {
   MOE_OK = 0,

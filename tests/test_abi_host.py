@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(declared) == set(abi.EXPORTS)
     for name in declared:
         assert hasattr(lib, name), name
-    assert abi.moe_abi_version() == 1
+    assert abi.moe_abi_version() == 2
 
 
 def test_status_strings(lib):
