@@ -317,6 +317,25 @@ def test_tensor_core_path_tiles(shape, w_dtype):
     check_output(inp, y, ids)
 
 
+# Shapes that put the FP8 GEMMs on CTA pairs (M = 256 over two SMs): routed
+# groups above 48 rows on average and d, f, f_s multiples of 256; ragged last
+# token tiles in every group, several 256-row weight tiles per group.
+PAIR_SHAPES = [
+    dict(T=200, d=512, E=16, k=4, f=256, fs=512),    # 50 rows / expert: TN 64 (gate/up), 128 (down)
+    dict(T=777, d=768, E=8, k=2, f=512, fs=256),     # 194 rows / expert, 3 down tiles of 256 rows
+]
+
+
+@pytest.mark.parametrize("act", [None, "e4m3"])
+@pytest.mark.parametrize("shape", PAIR_SHAPES, ids=[f"T{s['T']}_E{s['E']}" for s in PAIR_SHAPES])
+def test_cta_pair_tiles(shape, act):
+    inp = moe_synth.make_custom(x_dtype="bf16", w_dtype="e4m3", seed=shape["T"] + 3, **shape)
+    flags = abi.MOE_FLAG_ACT_E4M3 if act else 0
+    _, _, y, ids, w, offs = run_layer(inp, flags)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids, act=act)
+
+
 @pytest.mark.parametrize("name", ["decode", "100b_decode"])
 def test_tensor_core_matches_simt_closely(name):
     # both paths against each other: the exact activation encodings (two E4M3

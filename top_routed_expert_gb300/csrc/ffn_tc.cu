@@ -26,10 +26,22 @@
 //    token tile) -- no host read-back of the expert counts.
 //  * warp roles: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
 //    warps 2-9 = epilogue (two per TMEM sub-partition).
+//  * large batches run on CTA pairs (clusters of two, cta_group::2): one
+//    MMA covers M = 256 weight rows, each CTA staging its 128 rows and half
+//    of the token rows, so each SM reads half the B operand per MAC that a
+//    lone 128-row tile needs; the even CTA issues the MMAs of both.  There
+//    the two activation terms share one accumulator: the hi and lo MMAs are
+//    block-scaled FP8 MMAs (kind::mxf8f6f4) whose B scales are 2^0 and 2^-4,
+//    both exact, so each token takes one accumulator column instead of two
+//    and a token tile holds twice the tokens for the same TMEM.
 //  * every mbarrier wait is bounded; on expiry the kernel records
 //    MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and
 //    returns.
 #include <cuda.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -75,6 +87,7 @@ struct TcArgs {
   int routed_on, shared_on;    // which groups this launch computes (FfnPart)
   int TN;                      // token rows per tile; MMA N = TERMS*TN
   int stages, acc_bufs, tmem_cols;
+  int sf_col;                  // merged terms: first of the 24 TMEM columns of block scales
   uint64_t wait_ns;            // limit of every bounded wait
   int inject_drop;             // test hook: CTA 0 withholds its first "accumulator ready"
   unsigned* status;
@@ -93,22 +106,52 @@ struct __align__(16) TcCtrl {
   GroupTable gt;
 };
 
+// MMA N of a tile of `rows` token rows (TERMS B rows each) under the
+// launch's full width N: the rows rounded up to 16 (the MMA's N granule),
+// at most N.
+template <int TERMS>
+__device__ __forceinline__ int tile_n_t(int rows, int N) {
+  return min(N, (TERMS * rows + 15) & ~15);
+}
+
 // TERMS = activation terms per token row: 2 (exact split, default) or 1
 // (MOE_FLAG_ACT_E4M3).  The B operand holds TERMS adjacent rows per token.
-template <int MODE, int TERMS>
+// CG = CTAs per MMA: 1, or 2 for a CTA pair (launched as clusters of two)
+// whose weight tiles are 256 rows: CTA rank r of the pair stages rows
+// [128 r, 128 r + 128) of the tile and B rows [r N/2, (r+1) N/2), its TMA
+// copies complete on the even CTA's "full" barriers, the even CTA issues the
+// MMAs and its commits arrive on the barriers of both CTAs, and both
+// epilogues release an accumulator on the even CTA's "tempty" barrier.
+// MERGED (pairs with two terms): mapB views the hi rows and mapBL the lo
+// rows of the quantised activations (TN / 2 rows per CTA each); the MMA N is
+// the token count and the stage holds the CTA's hi tile, then its lo tile.
+template <int MODE, int TERMS, int CG>
 __global__ void __launch_bounds__(kTcThreads, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAS,
-              const __grid_constant__ CUtensorMap mapB, TcArgs a) {
-  constexpr int NA = (MODE == 1) ? 2 : 1;   // weight tiles per stage (gate + up, or down)
+              const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapBL, TcArgs a) {
+  constexpr bool PAIR = CG == 2;
+  constexpr bool MERGED = PAIR && TERMS == 2;
+  // merged gate/up: one 128-row A tile holds 64 features of gate and of up,
+  // interleaved by 16 rows, so one accumulator carries both
+  constexpr bool GU_IL = MERGED && MODE == 1;
+  constexpr int NA = (MODE == 1 && !GU_IL) ? 2 : 1;   // weight tiles per stage (gate + up, or one)
+  constexpr int ET = MERGED ? 1 : TERMS;    // accumulator columns per token
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int N = TERMS * a.TN;
-  const uint32_t b_bytes = static_cast<uint32_t>(N) * kBK;
+  const int N = ET * a.TN;                  // MMA N (the launch's widest)
+  const int brows = MERGED ? a.TN : N / CG;   // B rows staged by this CTA per stage
+  const uint32_t b_bytes = static_cast<uint32_t>(brows) * kBK;
+  const uint32_t lo_off = static_cast<uint32_t>(a.TN / 2) * kBK;   // merged: the lo tile after the hi tile
   const uint32_t stage_bytes = NA * kABytes + ((b_bytes + 1023u) & ~1023u);
   TcCtrl* c = reinterpret_cast<TcCtrl*>(smem + a.stages * stage_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.E + 1;
   volatile int* abort = &c->abort;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // CTA within the pair
+  auto tile_n = [](int rows, int n) { return tile_n_t<ET>(rows, n); };
+  const bool leader = rank == 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);   // worker index
+  const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -117,7 +160,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&c->tfull[b]), 1);
-      mbar_init(smem_u32(&c->tempty[b]), kEpiThreads);
+      mbar_init(smem_u32(&c->tempty[b]), CG * kEpiThreads);
     }
     mbar_init(smem_u32(&c->drain), 1);
     mbar_init(smem_u32(&c->ep_sync), kEpiThreads);
@@ -128,56 +171,109 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   // kernel reads what earlier kernels wrote
   pdl_enter();
   // device-side tile list: group g = expert (g < E) or the shared expert (g = E)
+  // (weight tiles of CG * 128 rows; interleaved gate/up: 128 features per pair)
+  constexpr int WT = GU_IL ? kBM : CG * kBM;
   if (MODE == 1)
-    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN, a.routed_on ? a.f / kBM : 0,
-                      a.shared_on ? a.fs / kBM : 0, a.status);
+    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN, a.routed_on ? a.f / WT : 0,
+                      a.shared_on ? a.fs / WT : 0, a.status);
   else
-    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN, a.routed_on ? a.d / kBM : 0,
-                      a.shared_on ? a.d / kBM : 0, a.status);
+    build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN, a.routed_on ? a.d / WT : 0,
+                      a.shared_on ? a.d / WT : 0, a.status);
   if (warp == 1) {
-    tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(&c->tmem_base), a.tmem_cols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mapA);
     tma_prefetch_desc(&mapAS);
     tma_prefetch_desc(&mapB);
+    if (MERGED) tma_prefetch_desc(&mapBL);
   }
   tc_fence_before();
-  __syncthreads();
+  // a pair: both CTAs' barriers are initialised and TMEM allocated before
+  // either CTA touches the other's
+  if constexpr (PAIR)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
   const int total = c->gt.tile_start[G];
+  if constexpr (MERGED) {
+    // block scales (UE8M0) in every lane of both CTAs: A 2^0 (4 columns),
+    // B 2^0 for the hi MMAs (8 columns), B 2^-4 for the lo MMAs (8 columns);
+    // the sub-partition of warp w is w % 4
+    if (warp >= 2 && warp < 6) {
+      const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t sf = tmem + lo + static_cast<uint32_t>(a.sf_col);
+      tmem_st_fill4(sf, 0x7F7F7F7Fu);
+      tmem_st_fill8(sf + 8, 0x7F7F7F7Fu);
+      tmem_st_fill8(sf + 16, 0x7B7B7B7Bu);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+  }
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
       int st = 0;
       uint32_t ph = 0, pending = 0, last_par = 0;
-      for (int i = blockIdx.x; i < total && !*abort; i += gridDim.x) {
+      for (int i = unit; i < total && !*abort; i += units) {
         const Tile t = decode_tile(c->gt, G, i, a.TN);
         const bool shr = t.g == a.E;
         const CUtensorMap* mA = shr ? &mapAS : &mapA;
+        const int rt = CG * t.wt + static_cast<int>(rank);   // this CTA's 128-row weight tile
         int arow0, arow1 = 0, K;
         if (MODE == 1) {
           const int width = shr ? a.fs : a.f;
           const int base = shr ? 0 : t.g * 2 * a.f;
-          arow0 = base + t.wt * kBM;
-          arow1 = base + width + t.wt * kBM;
+          arow0 = base + rt * kBM;
+          arow1 = base + width + rt * kBM;
           K = a.d;
         } else {
-          arow0 = (shr ? 0 : t.g * a.d) + t.wt * kBM;
+          arow0 = (shr ? 0 : t.g * a.d) + rt * kBM;
           K = shr ? a.fs : a.f;
         }
-        const int brow = TERMS * t.row0;
+        // the pair splits the tile's MMA N (its rows, rounded up to 16) evenly
+        const int brow = (MERGED ? 1 : TERMS) * t.row0 + static_cast<int>(rank) * (tile_n(t.nrows, N) / CG);
         for (int kb = 0; kb < K / kBK; ++kb) {
           if (!mbar_wait(smem_u32(&c->empty[st]), ph ^ 1u, abort, a.wait_ns)) break;
           const uint32_t full = smem_u32(&c->full[st]);
-          mbar_arrive_expect_tx(full, NA * kABytes + b_bytes);
           const uint32_t sA = smem_u32(smem + st * stage_bytes);
-          tma_load_2d(sA, mA, kb * kBK, arow0, full);
-          if (MODE == 1) tma_load_2d(sA + kABytes, mA, kb * kBK, arow1, full);
-          tma_load_2d(sA + NA * kABytes, &mapB, kb * kBK, brow, full);
+          if constexpr (PAIR) {
+            // the even CTA's barrier counts the bytes of both CTAs
+            if (leader) mbar_arrive_expect_tx(full, CG * (NA * kABytes + b_bytes));
+            const uint32_t fullc = mapa_shared(full, 0);
+            if constexpr (GU_IL) {
+              // sub-partition q (tile rows 32q..32q+31): 16 gate rows, then
+              // the 16 up rows of the same features (boxes of 16 rows)
+              const int width = shr ? a.fs : a.f;
+              const int frow = (shr ? 0 : t.g * 2 * a.f) + t.wt * kBM + static_cast<int>(rank) * 64;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                tma_load_2d_pair(sA + (32 * q) * kBK, mA, kb * kBK, frow + 16 * q, fullc);
+                tma_load_2d_pair(sA + (32 * q + 16) * kBK, mA, kb * kBK, frow + width + 16 * q, fullc);
+              }
+            } else {
+              tma_load_2d_pair(sA, mA, kb * kBK, arow0, fullc);
+              if (MODE == 1) tma_load_2d_pair(sA + kABytes, mA, kb * kBK, arow1, fullc);
+            }
+            tma_load_2d_pair(sA + NA * kABytes, &mapB, kb * kBK, brow, fullc);
+            if (MERGED) tma_load_2d_pair(sA + NA * kABytes + lo_off, &mapBL, kb * kBK, brow, fullc);
+          } else {
+            mbar_arrive_expect_tx(full, NA * kABytes + b_bytes);
+            tma_load_2d(sA, mA, kb * kBK, arow0, full);
+            if (MODE == 1) tma_load_2d(sA + kABytes, mA, kb * kBK, arow1, full);
+            tma_load_2d(sA + NA * kABytes, &mapB, kb * kBK, brow, full);
+          }
           pending |= 1u << st;
           last_par = (last_par & ~(1u << st)) | (ph << st);
           if (++st == a.stages) {
@@ -187,21 +283,34 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         }
       }
       // every issued copy must land before the CTA may exit
-      int no_abort = 0;
-      for (int s = 0; s < a.stages; ++s)
-        if (pending & (1u << s)) mbar_wait(smem_u32(&c->full[s]), (last_par >> s) & 1u, &no_abort, kDrainLimitNs);
+      if constexpr (PAIR) {
+        // A pair's copies complete on the even CTA's barriers.  Without an
+        // abort the MMAs consumed every one of them (so they have landed);
+        // after an abort, give copies still in flight 2 ms to land.
+        if (*abort) {
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
+        }
+      } else {
+        int no_abort = 0;
+        for (int s = 0; s < a.stages; ++s)
+          if (pending & (1u << s)) mbar_wait(smem_u32(&c->full[s]), (last_par >> s) & 1u, &no_abort, kDrainLimitNs);
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_f8_e4m3(kBM, N);
       int st = 0, ab = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+      for (int i = unit; i < total && ok; i += units) {
         const Tile t = decode_tile(c->gt, G, i, a.TN);
         const bool shr = t.g == a.E;
         const int K = (MODE == 1) ? a.d : (shr ? a.fs : a.f);
+        // MMA N of this tile: its rows (x terms) rounded up to 16, so a ragged
+        // last tile of a group costs no MMA work beyond that
+        const uint32_t idesc = MERGED ? idesc_mxf8_ue8m0(CG * kBM, tile_n(t.nrows, N))
+                                      : idesc_f8_e4m3(CG * kBM, tile_n(t.nrows, N));
         if (!mbar_wait(smem_u32(&c->tempty[ab]), aph ^ 1u, abort, a.wait_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + static_cast<uint32_t>(ab * NA * N);
@@ -216,28 +325,52 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           const uint64_t da0 = desc_sw128(sA);
           const uint64_t da1 = desc_sw128(sA + kABytes);
           const uint64_t db = desc_sw128(sA + NA * kABytes);
+          const uint64_t dbl = desc_sw128(sA + NA * kABytes + lo_off);
+          const uint32_t sfa = tmem + static_cast<uint32_t>(a.sf_col);
 #pragma unroll
           for (int kk = 0; kk < kBK / 32; ++kk) {
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            mma_f8f6f4(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
-            if (MODE == 1) mma_f8f6f4(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+            if constexpr (MERGED) {
+              mma_mxf8_pair(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum, sfa, sfa + 8);
+              mma_mxf8_pair(d0, da0 + 2 * kk, dbl + 2 * kk, idesc, 1u, sfa, sfa + 16);
+              if (MODE == 1 && !GU_IL) {
+                mma_mxf8_pair(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum, sfa, sfa + 8);
+                mma_mxf8_pair(d1, da1 + 2 * kk, dbl + 2 * kk, idesc, 1u, sfa, sfa + 16);
+              }
+            } else if constexpr (PAIR) {
+              mma_f8f6f4_pair(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
+              if (MODE == 1) mma_f8f6f4_pair(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+            } else {
+              mma_f8f6f4(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
+              if (MODE == 1) mma_f8f6f4(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum);
+            }
           }
-          mma_commit(smem_u32(&c->empty[st]));
+          if constexpr (PAIR)
+            mma_commit_pair(smem_u32(&c->empty[st]), 3);
+          else
+            mma_commit(smem_u32(&c->empty[st]));
           if (++st == a.stages) {
             st = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        if (!(a.inject_drop && blockIdx.x == 0 && i == static_cast<int>(blockIdx.x)))
-          mma_commit(smem_u32(&c->tfull[ab]));
+        if (!(a.inject_drop && unit == 0 && i == unit)) {
+          if constexpr (PAIR)
+            mma_commit_pair(smem_u32(&c->tfull[ab]), 3);
+          else
+            mma_commit(smem_u32(&c->tfull[ab]));
+        }
         if (++ab == a.acc_bufs) {
           ab = 0;
           aph ^= 1u;
         }
       }
       // no MMA may still be running when TMEM is released
-      mma_commit(smem_u32(&c->drain));
+      if constexpr (PAIR)
+        mma_commit_pair(smem_u32(&c->drain), 3);
+      else
+        mma_commit(smem_u32(&c->drain));
       int no_abort = 0;
       mbar_wait(smem_u32(&c->drain), 0, &no_abort, kDrainLimitNs);
     }
@@ -252,7 +385,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
     int ab = 0, cb_par = 0;
     uint32_t aph = 0, eph = 0;
-    for (int i = blockIdx.x; i < total; i += gridDim.x) {
+    for (int i = unit; i < total; i += units) {
       const Tile t = decode_tile(c->gt, G, i, a.TN);
       const bool shr = t.g == a.E;
       // Per-row coefficients of this tile, loaded while the MMAs run: the
@@ -284,27 +417,63 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       cb_par ^= 1;
       if (!mbar_wait(smem_u32(&c->tfull[ab]), aph, abort, a.wait_ns)) break;
       tc_fence_after();
-      const int col = t.wt * kBM + n;
-      if (MODE == 1) {
+      const int col = (CG * t.wt + static_cast<int>(rank)) * kBM + n;
+      if constexpr (GU_IL) {
+        // lanes 0-15 of the sub-partition hold gate, lanes 16-31 up, of the
+        // same 16 features; lane l < 16 finishes tokens c0..c0+15 of a chunk
+        // and lane l + 16 tokens c0+16..c0+31, after one exchange
+        const bool upper = lane >= 16;
+        const int fcol = t.wt * kBM + static_cast<int>(rank) * 64 + sub * 16 + (lane & 15);
+        const int width = shr ? a.fs : a.f;
+        const float sg = shr ? a.as_scale[fcol] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + fcol];
+        const float su =
+            shr ? a.as_scale[width + fcol] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + a.f + fcol];
+        const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
+        const int nt = tile_n(t.nrows, N);
+        for (int c0 = 32 * half; c0 < nt; c0 += 64) {
+          float v0[16], v1[16];
+          tmem_ld16x2(cb + c0, cb + c0 + 16, v0, v1);
+          float gg[16], uu[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float send = upper ? v0[j] : v1[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            gg[j] = upper ? recv : v0[j];
+            uu[j] = upper ? v1[j] : recv;
+          }
+          const int jb = c0 + (upper ? 16 : 0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = jb + j;
+            if (tok < t.nrows) {
+              const float cfj = coef[tok];
+              const float g = gg[j] * cfj * sg;
+              const float u = uu[j] * cfj * su;
+              a.h[static_cast<size_t>(t.row0 + tok) * a.fmax + fcol] = __float2bfloat16_rn(silu(g) * u);
+            }
+          }
+        }
+      } else if (MODE == 1) {
         const int width = shr ? a.fs : a.f;
         const float sg = shr ? a.as_scale[col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + col];
         const float su = shr ? a.as_scale[width + col] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + a.f + col];
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
-        // chunks of 32 columns = 32 / TERMS token rows; N is a multiple of
+        // chunks of 32 columns = 32 / ET token rows; N is a multiple of
         // 16 and a 32-wide load past N stays inside the allocation
-        constexpr int TPC = 32 / TERMS;
-        for (int c0 = 32 * half; c0 < N; c0 += 64) {
+        constexpr int TPC = 32 / ET;
+        const int nt = tile_n(t.nrows, N);
+        for (int c0 = 32 * half; c0 < nt; c0 += 64) {
           float gv[32], uv[32], cf[TPC];
 #pragma unroll
-          for (int jj = 0; jj < TPC; ++jj) cf[jj] = coef[c0 / TERMS + jj];
+          for (int jj = 0; jj < TPC; ++jj) cf[jj] = coef[c0 / ET + jj];
           tmem_ld32x2(cb + c0, cb + N + c0, gv, uv);
 #pragma unroll
           for (int jj = 0; jj < TPC; ++jj) {
-            const int j = c0 / TERMS + jj;
+            const int j = c0 / ET + jj;
             if (j < t.nrows) {
               const int row = t.row0 + j;
-              const float gd = TERMS == 2 ? gv[2 * jj] + gv[2 * jj + 1] * 0.0625f : gv[jj];
-              const float ud = TERMS == 2 ? uv[2 * jj] + uv[2 * jj + 1] * 0.0625f : uv[jj];
+              const float gd = ET == 2 ? gv[2 * jj] + gv[2 * jj + 1] * 0.0625f : gv[jj];
+              const float ud = ET == 2 ? uv[2 * jj] + uv[2 * jj + 1] * 0.0625f : uv[jj];
               const float g = gd * cf[jj] * sg;
               const float u = ud * cf[jj] * su;
               a.h[static_cast<size_t>(row) * a.fmax + col] = __float2bfloat16_rn(silu(g) * u);
@@ -316,36 +485,61 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
         void* outp = shr ? a.shared_out : a.out_perm;
         const size_t out0 = static_cast<size_t>(shr ? t.row0 - a.P : t.row0) * a.d + col;
-        // chunks of 64 columns = 64 / TERMS token rows
-        constexpr int TPC = 64 / TERMS;
-        for (int c0 = 64 * half; c0 < N; c0 += 128) {
-          float d0[32], d1[32];
-          float cf[TERMS == 2 ? TPC : 1];   // two terms: this chunk's coefficients in registers
-          if (TERMS == 2) {
+        // chunks of 64 columns = 64 / ET token rows
+        constexpr int TPC = 64 / ET;
+        const int nt = tile_n(t.nrows, N);
+        if constexpr (ET == 1) {
+          // one column per token: chunk c0 holds tokens c0..c0+63 (c0 < nt
+          // implies c0 < nrows); the output pointer steps one row per token
+          for (int c0 = 64 * half; c0 < nt; c0 += 128) {
+            float d0[32], d1[32];
+            tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
+            const int jn = min(64, t.nrows - c0);
+            const size_t first = out0 + static_cast<size_t>(c0) * a.d;
+            if (a.out_bf16) {
+              __nv_bfloat16* p = static_cast<__nv_bfloat16*>(outp) + first;
 #pragma unroll
-            for (int jj = 0; jj < TPC; ++jj) cf[jj] = coef[c0 / TERMS + jj];
+              for (int jj = 0; jj < 64; ++jj, p += a.d)
+                if (jj < jn) *p = __float2bfloat16_rn((jj < 32 ? d0[jj] : d1[jj - 32]) * coef[c0 + jj] * sw);
+            } else {
+              float* p = static_cast<float*>(outp) + first;
+#pragma unroll
+              for (int jj = 0; jj < 64; ++jj, p += a.d)
+                if (jj < jn) *p = (jj < 32 ? d0[jj] : d1[jj - 32]) * coef[c0 + jj] * sw;
+            }
+          }
+        } else
+        for (int c0 = 64 * half; c0 < nt; c0 += 128) {
+          float d0[32], d1[32];
+          float cf[ET == 2 ? TPC : 1];   // two terms: this chunk's coefficients in registers
+          if (ET == 2) {
+#pragma unroll
+            for (int jj = 0; jj < TPC; ++jj) cf[jj] = coef[c0 / ET + jj];
           }
           tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
 #pragma unroll
           for (int jj = 0; jj < TPC; ++jj) {
-            const int j = c0 / TERMS + jj;
+            const int j = c0 / ET + jj;
             if (j < t.nrows) {
               float dsum;
-              if (TERMS == 2) {
+              if (ET == 2) {
                 const float* dv = jj < 16 ? d0 : d1;
                 const int q = 2 * (jj & 15);
                 dsum = dv[q] + dv[q + 1] * 0.0625f;
               } else {
                 dsum = jj < 32 ? d0[jj] : d1[jj - 32];
               }
-              const float cfj = TERMS == 2 ? cf[TERMS == 2 ? jj : 0] : coef[j];
+              const float cfj = ET == 2 ? cf[ET == 2 ? jj : 0] : coef[j];
               store_out(outp, out0 + static_cast<size_t>(j) * a.d, dsum * cfj * sw, a.out_bf16);
             }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&c->tempty[ab]));
+      if constexpr (PAIR)
+        mbar_arrive_cluster(mapa_shared(smem_u32(&c->tempty[ab]), 0));
+      else
+        mbar_arrive(smem_u32(&c->tempty[ab]));
       if (++ab == a.acc_bufs) {
         ab = 0;
         aph ^= 1u;
@@ -354,9 +548,19 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   }
 
   tc_fence_before();
-  __syncthreads();
+  // a pair: neither CTA frees TMEM or exits while the pair's MMAs, copies or
+  // arrivals may still reach it
+  if constexpr (PAIR)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, a.tmem_cols);
+    else
+      tmem_dealloc(tmem, a.tmem_cols);
+  }
   if (threadIdx.x == 0 && c->abort) set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
 }
 
@@ -538,35 +742,99 @@ TcPlan plan(const moe_config_t& c) {
   return p;
 }
 
-template <int MODE, int TERMS>
-cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUtensorMap& mB, TcArgs a,
-                        int wtiles_routed, int wtiles_shared, int grid_cap, cudaStream_t stream) {
-  constexpr int NA = (MODE == 1) ? 2 : 1;
-  const int N = TERMS * a.TN;
-  const int stage_bytes = NA * kABytes + align_up(static_cast<size_t>(N) * kBK, 1024);
+// Most clusters of two CTAs of `kernel` (with `smem` bytes each) that the
+// GPU holds at once, cached per (kernel, smem, device).
+int max_pairs(const void* kernel, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, size_t, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_tuple(kernel, smem, dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+  cache[key] = n;
+  return n;
+}
+
+// wtiles_* = weight tiles per group, of CG * 128 rows.
+template <int MODE, int TERMS, int CG>
+cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUtensorMap& mB, const CUtensorMap& mBL,
+                        TcArgs a, int wtiles_routed, int wtiles_shared, int grid_cap, cudaStream_t stream) {
+  constexpr bool MERGED = CG == 2 && TERMS == 2;
+  constexpr int NA = (MODE == 1 && !MERGED) ? 2 : 1;   // merged gate/up: one interleaved A tile
+  const int N = (MERGED ? 1 : TERMS) * a.TN;
+  const int brows = MERGED ? a.TN : N / CG;
+  const int stage_bytes = NA * kABytes + align_up(static_cast<size_t>(brows) * kBK, 1024);
   // as many stages as fit next to the control block in 227 KB
   a.stages = std::min(kMaxStages, static_cast<int>((227 * 1024 - 1024 - sizeof(TcCtrl)) / stage_bytes));
   const int per_acc = NA * N;
   a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
   // The epilogue reads 32 columns per load (gemm1: gate and up from column c0
-  // and N + c0, c0 < N in steps of 32; gemm2: 64 from c0, c0 < N in steps of
-  // 64), so the allocation covers the last buffer plus that overhang.
+  // and N + c0, c0 < N in steps of 32, or one interleaved accumulator; gemm2:
+  // 64 from c0, c0 < N in steps of 64), so the allocation covers the last
+  // buffer plus that overhang.
   const int last = (a.acc_bufs - 1) * per_acc;
-  const int reach = (MODE == 1) ? last + N + (N + 31) / 32 * 32 : last + (N + 63) / 64 * 64;
+  const int reach = (MODE == 1) ? last + (NA == 2 ? N : 0) + (N + 31) / 32 * 32 : last + (N + 63) / 64 * 64;
   int cols = 32;
+  a.sf_col = 0;
+  if (MERGED) {
+    // 24 columns of block scales after the accumulators (the epilogue's
+    // overhanging loads may read them; they read past no allocation)
+    a.sf_col = align_up(static_cast<size_t>(a.acc_bufs * per_acc), 8);
+    cols = 512;
+    if (a.sf_col + 24 > 512 || reach > 512) return cudaErrorInvalidConfiguration;
+  }
   while (cols < reach) cols *= 2;
   if (cols > 512) return cudaErrorInvalidConfiguration;
   a.tmem_cols = cols;
   size_t smem = 1024 + static_cast<size_t>(a.stages) * stage_bytes + sizeof(TcCtrl);
   smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
-  cudaError_t err =
-      ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_tc_kernel<MODE, TERMS>), static_cast<int>(smem));
+  const void* kfn = reinterpret_cast<const void*>(ffn_tc_kernel<MODE, TERMS, CG>);
+  cudaError_t err = ensure_kernel_attrs(kfn, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const long long tiles_ub = (a.routed_on ? static_cast<long long>(wtiles_routed) * (a.P / a.TN + a.E) : 0) +
                              (a.shared_on ? static_cast<long long>(wtiles_shared) * ((a.T + a.TN - 1) / a.TN) : 0);
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(grid_cap, tiles_ub)));
+  if (CG == 1) {
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(grid_cap, tiles_ub)));
+    count_launches(1);
+    return launch_pdl(ffn_tc_kernel<MODE, TERMS, CG>, grid, kTcThreads, smem, stream, mA, mAS, mB, mBL, a);
+  }
+  // pairs: no more clusters than the GPU holds at once (each walks its share
+  // of the tile list in turn)
+  const int resident = max_pairs(kfn, smem);
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  const int pairs = static_cast<int>(
+      std::max<long long>(1, std::min<long long>(std::min(resident, std::max(1, grid_cap / 2)), tiles_ub)));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   count_launches(1);
-  return launch_pdl(ffn_tc_kernel<MODE, TERMS>, grid, kTcThreads, smem, stream, mA, mAS, mB, a);
+  return cudaLaunchKernelEx(&cfg, ffn_tc_kernel<MODE, TERMS, CG>, mA, mAS, mB, mBL, a);
 }
 
 }  // namespace
@@ -593,12 +861,28 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   // alone, from T (one group of T rows: the fewest tiles, so each weight tile
   // is read as few times as possible)
   const int tn = part.routed ? pl.TN : (T <= 8 ? 8 : T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128);
-  const int tn1 = one_term ? std::max(16, std::min(tn, 128)) : std::min(tn, MOE_TC_TN1_CAP);
+  int tn1 = one_term ? std::max(16, std::min(tn, 128)) : std::min(tn, MOE_TC_TN1_CAP);
   // one term, down GEMM: 256-token tiles once groups are that large (N = 256
   // halves the operand bytes per MAC of a 128 x 128 tile; K = f is short, so
   // the feed, not the MMA, bounds the smaller tile)
   const bool big = part.routed ? static_cast<double>(P) / E > 96 : T > 96;
-  const int tn2 = one_term ? (big ? 256 : std::max(16, std::min(tn, 128))) : std::min(tn, MOE_TC_TN2_CAP);
+  int tn2 = one_term ? (big ? 256 : std::max(16, std::min(tn, 128))) : std::min(tn, MOE_TC_TN2_CAP);
+  // CTA pairs (M = 256) for large batches, where the MMAs rather than the
+  // weight stream bound the GEMMs: average routed groups above 48 rows and
+  // widths that split into 256-row tiles.  With two terms the pair merges
+  // them into one accumulator and gate/up interleaves gate and up rows in
+  // one A tile: token tiles of 224 for both GEMMs (two accumulator buffers
+  // of 224 columns and the block scales fill TMEM), so each MMA has N = 224
+  // (an FP8 MMA with N <= 128 costs nearly as long as one with N = 224).
+  const bool inject = (c.flags & MOE_FLAG_INJECT_TIMEOUT) != 0;
+  const bool pair = P > 48 * E && f % 256 == 0 && fs % 256 == 0 && d % 256 == 0 && !inject &&
+                    (one_term ? tn1 >= 128 && tn2 >= 128 : true);
+  const bool merged = pair && !one_term;
+  if (merged) {
+    tn1 = 224;
+    tn2 = 224;
+  }
+  const int cg = pair ? 2 : 1;
   char* base = static_cast<char*>(ws);
   uint8_t* xq = reinterpret_cast<uint8_t*>(base + pl.xq);
   float* sx = reinterpret_cast<float*>(base + pl.sx);
@@ -618,7 +902,7 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
                                !one_term, r0, r1, status);
   if (err != cudaSuccess) return err;
 
-  CUtensorMap mA, mAS, mB;
+  CUtensorMap mA, mAS, mB, mBL;
   TcArgs a = {};
   a.offsets = offsets; a.sorted_pair = sorted_pair; a.topk_w = topk_w;
   a.h = h; a.out_perm = out_perm; a.shared_out = shared_out;
@@ -626,22 +910,38 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   a.T = T; a.k = k; a.E = E; a.P = P; a.d = d; a.f = f; a.fs = fs; a.fmax = fmax;
   a.routed_on = part.routed; a.shared_on = part.shared;
   a.TN = pl.TN; a.status = status;
-  const bool inject = (c.flags & MOE_FLAG_INJECT_TIMEOUT) != 0;
   a.wait_ns = inject ? 20000000ull : kWaitLimitNs;
   a.inject_drop = inject ? 1 : 0;
 
-  // gemm1: gate/up (B: both term rows of each activation row, or the hi rows only)
-  const bool mb_ok = one_term ? make_map(&mB, xq, static_cast<uint64_t>(R), d, tn1, 2 * static_cast<uint64_t>(d))
-                              : make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * tn1);
-  if (!make_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, kBM) ||
-      !make_map(&mAS, w->s13, static_cast<uint64_t>(2) * fs, d, kBM) || !mb_ok)
+  // gemm1: gate/up (B: both term rows of each activation row; the hi rows
+  // only; or, merged, the hi rows and the lo rows as two views)
+  bool mb_ok;
+  if (merged)
+    mb_ok = make_map(&mB, xq, static_cast<uint64_t>(R), d, tn1 / 2, 2 * static_cast<uint64_t>(d)) &&
+            make_map(&mBL, xq + d, static_cast<uint64_t>(R), d, tn1 / 2, 2 * static_cast<uint64_t>(d));
+  else
+    mb_ok = one_term ? make_map(&mB, xq, static_cast<uint64_t>(R), d, tn1 / cg, 2 * static_cast<uint64_t>(d))
+                     : make_map(&mB, xq, static_cast<uint64_t>(2) * R, d, 2 * tn1 / cg);
+  if (!merged) mBL = mB;
+  // (merged: gate and up rows are fetched in boxes of 16 rows, interleaved)
+  const uint32_t abox = merged ? 16 : kBM;
+  if (!make_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, abox) ||
+      !make_map(&mAS, w->s13, static_cast<uint64_t>(2) * fs, d, abox) || !mb_ok)
     return cudaErrorInvalidValue;
   a.a_scale = static_cast<const float*>(w->w13_scale);
   a.as_scale = static_cast<const float*>(w->s13_scale);
   a.b_scale = sx;
-  a.TN = tn1;   // two buffers of (gate, up) x TERMS*TN columns fit TMEM at TERMS*TN <= 128
-  err = one_term ? launch_gemm<1, 1>(mA, mAS, mB, a, f / kBM, fs / kBM, cap, stream)
-                 : launch_gemm<1, 2>(mA, mAS, mB, a, f / kBM, fs / kBM, cap, stream);
+  a.TN = tn1;   // two buffers of (gate, up) x (columns per token) x TN fit TMEM
+  // weight tiles per group: of cg * 128 rows, or, merged gate/up, of 128
+  // features (64 of gate and up per CTA)
+  const int wt_f = merged ? f / kBM : f / (cg * kBM), wt_fs = merged ? fs / kBM : fs / (cg * kBM);
+  const int wt_d = d / (cg * kBM);
+  if (pair)
+    err = one_term ? launch_gemm<1, 1, 2>(mA, mAS, mB, mBL, a, wt_f, wt_fs, cap, stream)
+                   : launch_gemm<1, 2, 2>(mA, mAS, mB, mBL, a, wt_f, wt_fs, cap, stream);
+  else
+    err = one_term ? launch_gemm<1, 1, 1>(mA, mAS, mB, mBL, a, wt_f, wt_fs, cap, stream)
+                   : launch_gemm<1, 2, 1>(mA, mAS, mB, mBL, a, wt_f, wt_fs, cap, stream);
   if (err != cudaSuccess) return err;
 
   count_launches(1);
@@ -651,9 +951,14 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   if (err != cudaSuccess) return err;
 
   // gemm2: down projection, gate weight, outputs
-  const bool mb2_ok = one_term
-                          ? make_map(&mB, hq, static_cast<uint64_t>(R), fmax, tn2, 2 * static_cast<uint64_t>(fmax))
-                          : make_map(&mB, hq, static_cast<uint64_t>(2) * R, fmax, 2 * tn2);
+  bool mb2_ok;
+  if (merged)
+    mb2_ok = make_map(&mB, hq, static_cast<uint64_t>(R), fmax, tn2 / 2, 2 * static_cast<uint64_t>(fmax)) &&
+             make_map(&mBL, hq + fmax, static_cast<uint64_t>(R), fmax, tn2 / 2, 2 * static_cast<uint64_t>(fmax));
+  else
+    mb2_ok = one_term ? make_map(&mB, hq, static_cast<uint64_t>(R), fmax, tn2 / cg, 2 * static_cast<uint64_t>(fmax))
+                      : make_map(&mB, hq, static_cast<uint64_t>(2) * R, fmax, 2 * tn2 / cg);
+  if (!merged) mBL = mB;
   if (!make_map(&mA, w->w2, static_cast<uint64_t>(E) * d, f, kBM) ||
       !make_map(&mAS, w->s2, static_cast<uint64_t>(d), fs, kBM) || !mb2_ok)
     return cudaErrorInvalidValue;
@@ -661,8 +966,11 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* x, const float* top
   a.as_scale = static_cast<const float*>(w->s2_scale);
   a.b_scale = sh;
   a.TN = tn2;
-  return one_term ? launch_gemm<2, 1>(mA, mAS, mB, a, d / kBM, d / kBM, cap, stream)
-                  : launch_gemm<2, 2>(mA, mAS, mB, a, d / kBM, d / kBM, cap, stream);
+  if (pair)
+    return one_term ? launch_gemm<2, 1, 2>(mA, mAS, mB, mBL, a, wt_d, wt_d, cap, stream)
+                    : launch_gemm<2, 2, 2>(mA, mAS, mB, mBL, a, wt_d, wt_d, cap, stream);
+  return one_term ? launch_gemm<2, 1, 1>(mA, mAS, mB, mBL, a, wt_d, wt_d, cap, stream)
+                  : launch_gemm<2, 2, 1>(mA, mAS, mB, mBL, a, wt_d, wt_d, cap, stream);
 }
 
 }  // namespace moe

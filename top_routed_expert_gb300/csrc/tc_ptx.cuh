@@ -88,6 +88,36 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, v
   }
 }
 
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster meets here (release / acquire at
+// cluster scope: shared-memory writes before it are visible to the peers after).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The shared::cluster address of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in a
+// peer CTA).  Release at CTA scope only: the arrival publishes no memory
+// writes to the peer (a cluster-scope release would first wait for every
+// global store the thread has in flight), it only says that this thread's
+// completed tcgen05.ld reads are done with a tensor-memory buffer.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -100,6 +130,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// The same load for a CTA pair: the copy lands in this CTA's shared memory
+// and completes its bytes on `bar_cluster`, an mbarrier of either CTA of the
+// pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
 }
 
@@ -204,6 +245,74 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr0, uint32_t taddr1, fl
   }
 }
 
+// CTA-pair forms (cta_group::2).  A kernel uses one cta_group throughout.
+// alloc / relinquish / dealloc are executed by one warp of each CTA of the
+// pair; the allocation sits at the same TMEM address in both.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// M = 256 over the pair, issued by the even CTA: rows 0-127 of A and the
+// first N/2 rows of B come from its shared memory, rows 128-255 of A and the
+// other N/2 rows of B from the odd CTA's (same offsets); D rows 0-127 land in
+// the even CTA's TMEM, rows 128-255 in the odd CTA's, all N columns each.
+__device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The block-scaled form (kind::mxf8f6f4, one UE8M0 scale per 32 K-elements
+// of each row of A and of B, read from TMEM at sfa / sfb): D (+)= (A * sa) (B * sb)^T.
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate, uint32_t sfa, uint32_t sfb) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+// Arrives once on the mbarrier at shared offset `bar` of each CTA in `mask`
+// when every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
+}
+
+// Stores one 32-bit value into 4 / 8 consecutive TMEM columns of this
+// thread's lane (32x32b shape: warp w reaches lanes 32 (w % 4) .. + 31).
+__device__ __forceinline__ void tmem_st_fill4(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %1, %1, %1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_fill8(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(taddr), "r"(v)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor of a K-major operand tile stored with the
 // 128-byte swizzle: 8-row x 128-byte atoms, 1024 bytes apart (SBO); the
 // leading-dimension offset is unused for this layout.  Bits: start address
@@ -224,6 +333,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 // [7,10) = 0 (E4M3), B format [10,13) = 0, N >> 3 in [17,23), M >> 4 in [24,29).
 __host__ __device__ __forceinline__ uint32_t idesc_f8_e4m3(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor of a block-scaled kind::mxf8f6f4 MMA: A and B E4M3
+// (format 0 in [7,10) and [10,13)), both K-major, N >> 3 in [17,23), scale
+// type UE8M0 (bit 23 = 1), M >> 4 in [24,29), scale-factor byte ids 0.
+__host__ __device__ __forceinline__ uint32_t idesc_mxf8_ue8m0(int M, int N) {
+  return (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 }  // namespace ptx
