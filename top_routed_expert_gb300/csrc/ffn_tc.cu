@@ -51,8 +51,13 @@ namespace moe {
 
 using namespace ptx;
 
-constexpr int kTcThreads = 320;          // producer, MMA, 8 epilogue warps
-constexpr int kEpiThreads = 256;
+// Warps: producer, MMA issuer, then the epilogue warps -- 8, or 16 for the
+// CTA-pair down projection, whose epilogue (one fp32 store per output
+// element) is the slowest part of a tile and needs more stores in flight.
+template <int MODE, int CG>
+__host__ __device__ constexpr int tc_epi_warps() { return (MODE == 2 && CG == 2) ? 16 : 8; }
+template <int MODE, int CG>
+__host__ __device__ constexpr int tc_threads() { return 64 + 32 * tc_epi_warps<MODE, CG>(); }
 constexpr int kBK = 128;                // K bytes (= FP8 elements) per pipeline stage
 constexpr int kBM = 128;                // weight rows per tile = MMA M
 constexpr int kMaxStages = 8;
@@ -126,7 +131,7 @@ __device__ __forceinline__ int tile_n_t(int rows, int N) {
 // rows of the quantised activations (TN / 2 rows per CTA each); the MMA N is
 // the token count and the stage holds the CTA's hi tile, then its lo tile.
 template <int MODE, int TERMS, int CG>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(tc_threads<MODE, CG>(), 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAS,
               const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapBL, TcArgs a) {
   constexpr bool PAIR = CG == 2;
@@ -135,6 +140,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   // interleaved by 16 rows, so one accumulator carries both
   constexpr bool GU_IL = MERGED && MODE == 1;
   constexpr int NA = (MODE == 1 && !GU_IL) ? 2 : 1;   // weight tiles per stage (gate + up, or one)
+  constexpr int kEpiThreads = 32 * tc_epi_warps<MODE, CG>();
+  constexpr int kParts = tc_epi_warps<MODE, CG>() / 4;   // epilogue warps per TMEM sub-partition
   constexpr int ET = MERGED ? 1 : TERMS;    // accumulator columns per token
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -379,7 +386,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     // Two warps per TMEM sub-partition (warp % 4 selects the 32 lanes a warp
     // may read); the pair of warps splits the tile's column chunks.
     const int sub = warp & 3;
-    const int half = (warp - 2) >> 2;               // 0 or 1
+    const int part = (warp - 2) >> 2;               // 0 .. kParts-1: splits the column chunks
     const int n = sub * 32 + lane;                  // weight row within the tile
     const int et = threadIdx.x - 64;                // 0..255 across the epilogue warps
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
@@ -430,7 +437,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             shr ? a.as_scale[width + fcol] : a.a_scale[static_cast<size_t>(t.g) * 2 * a.f + a.f + fcol];
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
         const int nt = tile_n(t.nrows, N);
-        for (int c0 = 32 * half; c0 < nt; c0 += 64) {
+        for (int c0 = 32 * part; c0 < nt; c0 += 32 * kParts) {
           float v0[16], v1[16];
           tmem_ld16x2(cb + c0, cb + c0 + 16, v0, v1);
           float gg[16], uu[16];
@@ -462,7 +469,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         // 16 and a 32-wide load past N stays inside the allocation
         constexpr int TPC = 32 / ET;
         const int nt = tile_n(t.nrows, N);
-        for (int c0 = 32 * half; c0 < nt; c0 += 64) {
+        for (int c0 = 32 * part; c0 < nt; c0 += 32 * kParts) {
           float gv[32], uv[32], cf[TPC];
 #pragma unroll
           for (int jj = 0; jj < TPC; ++jj) cf[jj] = coef[c0 / ET + jj];
@@ -491,7 +498,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         if constexpr (ET == 1) {
           // one column per token: chunk c0 holds tokens c0..c0+63 (c0 < nt
           // implies c0 < nrows); the output pointer steps one row per token
-          for (int c0 = 64 * half; c0 < nt; c0 += 128) {
+          for (int c0 = 64 * part; c0 < nt; c0 += 64 * kParts) {
             float d0[32], d1[32];
             tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
             const int jn = min(64, t.nrows - c0);
@@ -509,7 +516,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
             }
           }
         } else
-        for (int c0 = 64 * half; c0 < nt; c0 += 128) {
+        for (int c0 = 64 * part; c0 < nt; c0 += 64 * kParts) {
           float d0[32], d1[32];
           float cf[ET == 2 ? TPC : 1];   // two terms: this chunk's coefficients in registers
           if (ET == 2) {
@@ -744,7 +751,7 @@ TcPlan plan(const moe_config_t& c) {
 
 // Most clusters of two CTAs of `kernel` (with `smem` bytes each) that the
 // GPU holds at once, cached per (kernel, smem, device).
-int max_pairs(const void* kernel, size_t smem) {
+int max_pairs(const void* kernel, size_t smem, int threads) {
   static std::mutex mu;
   static std::map<std::tuple<const void*, size_t, int>, int> cache;
   int dev = 0;
@@ -755,7 +762,7 @@ int max_pairs(const void* kernel, size_t smem) {
   if (it != cache.end()) return it->second;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -811,17 +818,18 @@ cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const CUt
   if (CG == 1) {
     const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(grid_cap, tiles_ub)));
     count_launches(1);
-    return launch_pdl(ffn_tc_kernel<MODE, TERMS, CG>, grid, kTcThreads, smem, stream, mA, mAS, mB, mBL, a);
+    return launch_pdl(ffn_tc_kernel<MODE, TERMS, CG>, grid, tc_threads<MODE, CG>(), smem, stream, mA, mAS, mB, mBL,
+                      a);
   }
   // pairs: no more clusters than the GPU holds at once (each walks its share
   // of the tile list in turn)
-  const int resident = max_pairs(kfn, smem);
+  const int resident = max_pairs(kfn, smem, tc_threads<MODE, CG>());
   if (resident < 1) return cudaErrorInvalidConfiguration;
   const int pairs = static_cast<int>(
       std::max<long long>(1, std::min<long long>(std::min(resident, std::max(1, grid_cap / 2)), tiles_ub)));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(tc_threads<MODE, CG>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
