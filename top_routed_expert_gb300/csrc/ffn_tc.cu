@@ -155,7 +155,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   const int G = a.E + 1;
   volatile int* abort = &c->abort;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // CTA within the pair
-  auto tile_n = [](int rows, int n) { return tile_n_t<ET>(rows, n); };
+  // per-tile MMA N on the pair path (its large-batch tiles are often
+  // ragged); the one-CTA path keeps the launch's N, which measured faster at
+  // decode, where a tile's rows fill one 16-column granule anyway
+  auto tile_n = [](int rows, int n) { return PAIR ? tile_n_t<ET>(rows, n) : n; };
   const bool leader = rank == 0;
   const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);   // worker index
   const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
