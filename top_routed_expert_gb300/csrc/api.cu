@@ -280,6 +280,36 @@ bool overlap_shared_expert(const moe_config_t& c) {
   return !(c.flags & MOE_FLAG_NO_OVERLAP) && static_cast<double>(c.T) * c.top_k <= 16.0 * c.n_experts;
 }
 
+// L2 warm-up of the routed gate/up weights that the GEMM's first wave reads.
+// A decode batch routes to nearly every expert, and the grouped GEMM's tile
+// list starts at expert 0, so its first wave streams the start of w13; the
+// routing in front of it moves almost nothing through HBM.  Prefetching that
+// start into L2 on the side stream while the router runs turns those reads
+// into L2 hits.  Each thread issues bulk prefetches of 64 KB pieces.  128 MB
+// measured best on the 8-GB decode layer (0.2857 -> 0.2844 ms per step, three
+// interleaved runs each; 48 and 96 MB were within noise of none).
+#ifndef MOE_L2_PREFETCH_MB
+#define MOE_L2_PREFETCH_MB 128
+#endif
+
+__global__ void l2_prefetch_kernel(const char* base, size_t bytes) {
+  constexpr size_t kPiece = 64 * 1024;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x * kPiece;
+  for (size_t off = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kPiece; off < bytes;
+       off += stride) {
+    const uint32_t n = static_cast<uint32_t>(bytes - off < kPiece ? bytes - off : kPiece);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(base + off)), "r"(n)
+                 : "memory");
+  }
+}
+
+// Bytes of routed gate/up weights to warm (a multiple of 16, at most w13).
+size_t l2_prefetch_bytes(const moe_config_t& c) {
+  const size_t w13 = static_cast<size_t>(c.n_experts) * 2 * c.d_ff * c.d_model / (c.w_dtype == MOE_NVFP4 ? 2 : 1);
+  const size_t want = static_cast<size_t>(MOE_L2_PREFETCH_MB) << 20;
+  return (want < w13 ? want : w13) & ~static_cast<size_t>(15);
+}
+
 }  // namespace
 
 namespace moe {
@@ -447,8 +477,15 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const flo
     routed_part.shared = false;
     if (cudaEventRecord(di.fork, s) != cudaSuccess || cudaStreamWaitEvent(di.side, di.fork, 0) != cudaSuccess)
       return MOE_ERR_CUDA;
-    st = run_expert_ffn(*cfg, x, w, offsets, sorted_pair, weights, out_perm, shared_out, scratch, di, shared_part,
-                        di.side);
+    const size_t warm = (path == kSimt) ? 0 : l2_prefetch_bytes(*cfg);
+    if (warm) {
+      count_launches(1);
+      l2_prefetch_kernel<<<16, 128, 0, di.side>>>(static_cast<const char*>(weights->w13), warm);
+      st = cuda_status(cudaGetLastError());
+    }
+    if (st == MOE_OK)
+      st = run_expert_ffn(*cfg, x, w, offsets, sorted_pair, weights, out_perm, shared_out, scratch, di, shared_part,
+                          di.side);
     // the join is recorded and awaited on every path, so a capture stays whole
     const bool joined = cudaEventRecord(di.join, di.side) == cudaSuccess;
     if (st == MOE_OK) st = moe_route(cfg, x, w_router, expert_bias, ids, w, rscratch, rscratch_bytes, stream);
