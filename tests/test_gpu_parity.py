@@ -305,6 +305,7 @@ TC_SHAPES = [
     dict(T=100, d=384, E=16, k=2, f=256, fs=128),    # 12.5              -> TN 32
     dict(T=160, d=256, E=16, k=4, f=128, fs=128),    # 40                -> TN 64
     dict(T=301, d=384, E=16, k=4, f=256, fs=384),    # 75                -> TN 128
+    dict(T=500, d=384, E=8, k=4, f=256, fs=128),     # 250: TN 128 (FP8), 256 (NVFP4 f16 rebuild)
 ]
 
 

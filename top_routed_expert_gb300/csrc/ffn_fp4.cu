@@ -88,7 +88,7 @@ struct __align__(16) F4Ctrl {
   uint64_t ep_sync;
   uint32_t tmem_base;
   int abort;
-  float coef[2][kF4BM];
+  float coef[2][2 * kF4BM];        // per token row (TN <= 256), by tile parity
   GroupTable gt;
 };
 
@@ -341,10 +341,10 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
       const Tile t = decode_tile(c->gt, G, i, a.TN);
       const bool shr = t.g == a.E;
-      {
+      for (int j = et; j < a.TN; j += kF4Epi) {
         float cf = 0.f;
-        if (et < t.nrows) {
-          const int row = t.row0 + et;
+        if (j < t.nrows) {
+          const int row = t.row0 + j;
           cf = a.b_scale[row] * (shr ? a.sg[0] : a.wg[t.g]);
           if (MODE == 2 && !shr) {
             const int p = a.sorted_pair[row];
@@ -356,7 +356,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
             }
           }
         }
-        c->coef[cb_par][et] = cf;
+        c->coef[cb_par][j] = cf;
       }
       mbar_arrive(smem_u32(&c->ep_sync));
       if (!mbar_wait_sleep(smem_u32(&c->ep_sync), eph, abort, kF4WaitNs, kF4IdleSleepNs)) break;
@@ -670,7 +670,11 @@ F4Plan f4_plan(const moe_config_t& c) {
   p.sh = take(4 * R);
   p.total = o;
   const double avg = static_cast<double>(P) / c.n_experts;
-  p.TN = avg <= 12 ? 16 : avg <= 24 ? 32 : avg <= 48 ? 64 : 128;
+  // 256-token tiles once the groups are that large: an f16 MMA of N = 128
+  // costs nearly as long as one of N = 256 (about 105 against 135 cycles),
+  // and each converted weight row then serves twice the tokens (the gate/up
+  // accumulators, 2 x 256 columns, fill TMEM and run single-buffered)
+  p.TN = avg <= 12 ? 16 : avg <= 24 ? 32 : avg <= 48 ? 64 : avg <= 192 ? 128 : 256;
   return p;
 }
 
@@ -685,9 +689,13 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
   // three f16 weight stages; activation slots for about 32 KB (at least 3,
   // at most 8); the rest of the budget goes to the raw ring, which hides HBM
   // latency
+  // (256-token gate/up tiles: two 32 KB activation slots, so that three raw
+  // slots still fit)
   a.stages = kF4MaxStages;
   a.bslots = std::max(3, std::min(kF4MaxB, 32768 / b_slot));
-  a.raw_slots = std::min(kF4MaxRaw, (kF4SmemBudget - a.stages * stage_bytes - a.bslots * b_slot) / raw_slot);
+  auto raw_fit = [&] { return (kF4SmemBudget - a.stages * stage_bytes - a.bslots * b_slot) / raw_slot; };
+  while (raw_fit() < 3 && a.bslots > 2) --a.bslots;
+  a.raw_slots = std::min(kF4MaxRaw, raw_fit());
   if (a.raw_slots < 2) return cudaErrorInvalidConfiguration;
   const int per_acc = NA * N;
   a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
