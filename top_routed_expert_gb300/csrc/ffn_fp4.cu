@@ -13,6 +13,12 @@
 // weight scale and the row scale (times the gate weight in the down
 // projection) are applied in the epilogue.
 //
+// Gate/up tiles interleave the two projections: the 128 weight rows of a
+// tile are, per 32-row TMEM sub-partition, 16 gate rows and the 16 up rows of
+// the same features (64 features per tile), so one accumulator holds both,
+// two of them fit TMEM at 256 tokens, and an epilogue lane pairs gate with
+// up through one exchange with the lane 16 away.
+//
 // Warp roles (480 threads): warp 0 issues the TMA loads of the activation
 // tiles into a ring of their own (up to 8 slots, so that the small decode
 // tiles are fetched well ahead of the MMA), warp 1 owns TMEM and issues the
@@ -181,15 +187,16 @@ __device__ __forceinline__ void cursor_next(KbCursor& cu, const GroupTable& gt, 
   }
 }
 
-// Row (within its tensor map: routed or shared weights) of weight tile
-// `a_idx` (0 = gate / down, 1 = up) of this tile, and its K.
+// First row (within its tensor map: routed or shared weights) of this tile's
+// weights, and its K: gate/up -- the tile's 64 gate rows (a_idx = 0) or its
+// 64 up rows (a_idx = 1); down -- its 128 rows.
 template <int MODE>
 __device__ __forceinline__ int weight_row(const F4Args& a, const Tile& t, int a_idx, int* K) {
   const bool shr = t.g == a.E;
   if (MODE == 1) {
     const int width = shr ? a.fs : a.f;
     *K = a.d;
-    return (shr ? 0 : t.g * 2 * a.f) + (a_idx ? width : 0) + t.wt * kF4BM;
+    return (shr ? 0 : t.g * 2 * a.f) + (a_idx ? width : 0) + t.wt * (kF4BM / 2);
   }
   *K = shr ? a.fs : a.f;
   return (shr ? 0 : t.g * a.d) + t.wt * kF4BM;
@@ -199,7 +206,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kF4Threads, 1)
 ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapA,
                const __grid_constant__ CUtensorMap mapAs, F4Args a) {
-  constexpr int NA = (MODE == 1) ? 2 : 1;
+  constexpr int NA = 1;   // one weight tile per stage (gate/up interleaved in it)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int N = a.TN;                                   // one f16 column per token
@@ -237,9 +244,9 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
     fence_barrier_init();
   }
   pdl_enter();   // from here on the kernel reads what earlier kernels wrote
-  if (MODE == 1)
+  if (MODE == 1)   // 64 features per tile
     build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN,
-                      a.routed_on ? a.f / kF4BM : 0, a.shared_on ? a.fs / kF4BM : 0, a.status);
+                      a.routed_on ? a.f / (kF4BM / 2) : 0, a.shared_on ? a.fs / (kF4BM / 2) : 0, a.status);
   else
     build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN,
                       a.routed_on ? a.d / kF4BM : 0, a.shared_on ? a.d / kF4BM : 0, a.status);
@@ -290,7 +297,6 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
         if (!mbar_wait(smem_u32(&c->tempty[ab]), aph ^ 1u, abort, kF4WaitNs)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + static_cast<uint32_t>(ab * NA * N);
-        const uint32_t d1 = d0 + static_cast<uint32_t>(N);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(smem_u32(&c->bfull[bs]), bph, abort, kF4WaitNs) ||
               !mbar_wait(smem_u32(&c->aready[st]), ph, abort, kF4WaitNs)) {
@@ -300,13 +306,11 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + st * stage_bytes);
           const uint64_t da0 = desc_sw128(sA);
-          const uint64_t da1 = desc_sw128(sA + kF4ATile);
           const uint64_t db = desc_sw128(smem_u32(bring + bs * b_slot));
 #pragma unroll
           for (int kk = 0; kk < kF4BK / 16; ++kk) {
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             mma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
-            if (MODE == 1) mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum);
           }
           mma_commit(smem_u32(&c->empty[st]));
           mma_commit(smem_u32(&c->bempty[bs]));
@@ -367,16 +371,31 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
       tc_fence_after();
       const int col = t.wt * kF4BM + n;
       if (MODE == 1) {
-        const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
-        for (int c0 = 0; c0 < N; c0 += 16) {       // 16 tokens per chunk
-          float gv[16], uv[16];
-          tmem_ld16x2(cb + c0, cb + N + c0, gv, uv);
+        // lanes 0-15 hold gate, lanes 16-31 up, of features fb .. fb+15; per
+        // 32-column chunk lane l < 16 finishes tokens c0 .. c0+15 and lane
+        // l + 16 tokens c0+16 .. c0+31 after one exchange
+        const bool upper = lane >= 16;
+        const int fcol = t.wt * (kF4BM / 2) + sub * 16 + (lane & 15);
+        const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
+        for (int c0 = 0; c0 < N; c0 += 32) {
+          float v0[16], v1[16];
+          tmem_ld16x2(cb + c0, cb + c0 + 16, v0, v1);
+          float gg[16], uu[16];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = c0 + jj;
-            if (j < t.nrows) {
-              const float cf = coef[j];
-              a.h[static_cast<size_t>(t.row0 + j) * a.fmax + col] = __float2bfloat16_rn(silu(gv[jj] * cf) * (uv[jj] * cf));
+          for (int j = 0; j < 16; ++j) {
+            const float send = upper ? v0[j] : v1[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            gg[j] = upper ? recv : v0[j];
+            uu[j] = upper ? v1[j] : recv;
+          }
+          const int jb = c0 + (upper ? 16 : 0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = jb + j;
+            if (tok < t.nrows) {
+              const float cf = coef[tok];
+              a.h[static_cast<size_t>(t.row0 + tok) * a.fmax + fcol] =
+                  __float2bfloat16_rn(silu(gg[j] * cf) * (uu[j] * cf));
             }
           }
         }
@@ -406,13 +425,12 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
     }
   } else if (warp < 6 + kF4ConvWarps) {
     // -------------------------------------------------- weight converters (warps 6..13)
-    // gate/up (two weight tiles): thread -> one row of one tile; down (one
-    // tile): two threads per row, four 16-byte f16 chunks each
+    // two threads per raw row, four 16-byte f16 chunks each
     const int ct = threadIdx.x - 192;                 // 0..255
     const int r = ct & (kF4BM - 1);
-    const int ai = (NA == 2) ? (ct >> 7) : 0;
-    constexpr int kChunks = (NA == 2) ? 8 : 4;        // f16 chunks (8 elements) per thread and stage
-    const int c_lo = (NA == 2) ? 0 : 4 * (ct >> 7);
+    constexpr int ai = 0;
+    constexpr int kChunks = 4;                        // f16 chunks (8 elements) per thread and stage
+    const int c_lo = 4 * (ct >> 7);
     const int sw = (r >> 1) & 3;                      // 64-byte swizzle of the raw code rows
     KbCursor conv;
     cursor_begin<MODE>(conv, c->gt, G, total, a);
@@ -426,7 +444,12 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
       const uint8_t* codes = slot + ai * kF4RawCodes + r * (kF4RK / 2);
       const uint32_t scw = *reinterpret_cast<const uint32_t*>(slot + NA * kF4RawCodes + ai * kF4RawScales +
                                                               r * (kF4RK / 16) + half * 4);
-      uint8_t* dst_row = smem + st * stage_bytes + ai * kF4ATile + r * 128;
+      // gate/up: raw rows 0-63 are gate features, 64-127 up features; tile row
+      // 32 q + i holds gate feature 16 q + i (i < 16), 32 q + 16 + i up
+      // feature 16 q + i (r and its tile row agree mod 16, so the swizzle is
+      // the same)
+      const int rd = (MODE == 1) ? ((r & 63) >> 4) * 32 + (r >> 6) * 16 + (r & 15) : r;
+      uint8_t* dst_row = smem + st * stage_bytes + ai * kF4ATile + rd * 128;
 #pragma unroll
       for (int q = 0; q < kChunks / 4; ++q) {
         const int lc = 2 * half + (c_lo >> 2) + q;    // logical 16-byte chunk of the 64-byte code row
@@ -475,24 +498,25 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
       const uint32_t slot = smem_u32(raw + rs * raw_slot);
       const uint32_t bar = smem_u32(&c->rfull[rs]);
       const int rb = cu.kb >> 1;                      // raw block within the row
+      // gate/up: two boxes of 64 rows (gate, then up) fill the slot's 128
+      // raw rows; down: one box of 128 rows
+      constexpr int kParts = (MODE == 1) ? 2 : 1;
+      constexpr int kRowsPer = kF4BM / kParts;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar, NA * kF4RawCodes);
-        for (int t2 = 0; t2 < NA; ++t2) {
+        mbar_arrive_expect_tx(bar, kF4RawCodes);
+        for (int p2 = 0; p2 < kParts; ++p2) {
           int K;
-          const int row = weight_row<MODE>(a, cu.t, t2, &K);
-          tma_load_2d(slot + t2 * kF4RawCodes, shr ? &mapAs : &mapA, rb * (kF4RK / 2), row, bar);
+          const int row = weight_row<MODE>(a, cu.t, p2, &K);
+          tma_load_2d(slot + p2 * kRowsPer * (kF4RK / 2), shr ? &mapAs : &mapA, rb * (kF4RK / 2), row, bar);
         }
       }
-      for (int t2 = 0; t2 < NA; ++t2) {
-        int K;
-        const int row = weight_row<MODE>(a, cu.t, t2, &K);
-        const uint8_t* sc = (shr ? a.ssc : a.wsc) + static_cast<size_t>(row) * (K / 16) + rb * (kF4RK / 16);
 #pragma unroll
-        for (int j = 0; j < kF4BM / 32; ++j) {
-          const int rr = lane + 32 * j;
-          cp_async8(slot + NA * kF4RawCodes + t2 * kF4RawScales + rr * (kF4RK / 16),
-                    sc + static_cast<size_t>(rr) * (K / 16));
-        }
+      for (int j = 0; j < kF4BM / 32; ++j) {
+        const int rr = lane + 32 * j;
+        int K;
+        const int row = weight_row<MODE>(a, cu.t, rr / kRowsPer, &K) + rr % kRowsPer;
+        const uint8_t* sc = (shr ? a.ssc : a.wsc) + static_cast<size_t>(row) * (K / 16) + rb * (kF4RK / 16);
+        cp_async8(slot + kF4RawCodes + rr * (kF4RK / 16), sc);
       }
       cp_async_arrive_noinc(bar);
       pending |= 1u << rs;
@@ -640,12 +664,12 @@ bool make_f16_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
 
 // Packed e2m1 codes [rows][K/2] bytes: box of 64 bytes (128 elements) x 128
 // rows, stored with the 64-byte swizzle.
-bool make_code_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+bool make_code_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
   EncodeTiledFn fn = f4_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {K / 2, rows};
   cuuint64_t strides[1] = {K / 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kF4RK / 2), static_cast<cuuint32_t>(kF4BM)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kF4RK / 2), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -681,7 +705,7 @@ F4Plan f4_plan(const moe_config_t& c) {
 template <int MODE>
 cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const CUtensorMap& mAs, F4Args a,
                            int wtiles_routed, int wtiles_shared, int grid_cap, cudaStream_t stream) {
-  constexpr int NA = (MODE == 1) ? 2 : 1;
+  constexpr int NA = 1;   // one (gate/up interleaved, or down) weight tile per stage
   const int N = a.TN;
   const int stage_bytes = NA * kF4ATile;
   const int b_slot = static_cast<int>(align_up(static_cast<size_t>(N) * 128, 1024));
@@ -699,9 +723,9 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
   if (a.raw_slots < 2) return cudaErrorInvalidConfiguration;
   const int per_acc = NA * N;
   a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
-  // epilogue loads: gemm1 16 columns at c0 and N + c0; gemm2 32 columns at c0
+  // epilogue loads: 32 columns at c0, c0 < N in steps of 32
   const int last = (a.acc_bufs - 1) * per_acc;
-  const int reach = (MODE == 1) ? last + N + (N + 15) / 16 * 16 : last + (N + 31) / 32 * 32;
+  const int reach = last + (N + 31) / 32 * 32;
   int cols = 32;
   while (cols < reach) cols *= 2;
   if (cols > 512) return cudaErrorInvalidConfiguration;
@@ -767,13 +791,13 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   CUtensorMap mB, mA, mAs;
   // gemm1: gate / up
   if (!make_f16_map(&mB, xh, R, d, d, a.TN) ||
-      !make_code_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d) ||
-      !make_code_map(&mAs, w->s13, 2 * static_cast<uint64_t>(fs), d))
+      !make_code_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, kF4BM / 2) ||
+      !make_code_map(&mAs, w->s13, 2 * static_cast<uint64_t>(fs), d, kF4BM / 2))
     return cudaErrorInvalidValue;
   a.wsc = static_cast<const uint8_t*>(w->w13_scale); a.wg = w->w13_gscale;
   a.ssc = static_cast<const uint8_t*>(w->s13_scale); a.sg = w->s13_gscale;
   a.b_scale = sx;
-  err = launch_f4_gemm<1>(mB, mA, mAs, a, f / kF4BM, fs / kF4BM, cap, stream);
+  err = launch_f4_gemm<1>(mB, mA, mAs, a, f / (kF4BM / 2), fs / (kF4BM / 2), cap, stream);
   if (err != cudaSuccess) return err;
 
   count_launches(1);
@@ -784,8 +808,8 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
 
   // gemm2: down projection, gate weight, outputs
   if (!make_f16_map(&mB, hh, R, fmax, fmax, a.TN) ||
-      !make_code_map(&mA, w->w2, static_cast<uint64_t>(E) * d, f) ||
-      !make_code_map(&mAs, w->s2, static_cast<uint64_t>(d), fs))
+      !make_code_map(&mA, w->w2, static_cast<uint64_t>(E) * d, f, kF4BM) ||
+      !make_code_map(&mAs, w->s2, static_cast<uint64_t>(d), fs, kF4BM))
     return cudaErrorInvalidValue;
   a.wsc = static_cast<const uint8_t*>(w->w2_scale); a.wg = w->w2_gscale;
   a.ssc = static_cast<const uint8_t*>(w->s2_scale); a.sg = w->s2_gscale;
