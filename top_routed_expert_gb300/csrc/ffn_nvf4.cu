@@ -31,9 +31,11 @@
 // step kk gets its own 4-column group: A at base + 16 a + 4 kk (weight tile
 // a), B at base + 32 + 4 kk.
 //
-// Warp roles (448 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
-// issuer, warps 2-9 epilogue (two per TMEM quadrant), warps 10-13 block-scale
-// writers (one per quadrant).  Persistent CTAs walk the device-built tile
+// Warp roles (704 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
+// issuer, warps 2-17 epilogue (four per TMEM quadrant, splitting the column
+// chunks: with fewer, a large batch's epilogue -- one term per token, an
+// output store per element -- kept the MMA waiting for free accumulators a
+// third of the time), warps 18-21 block-scale writers (one per quadrant).  Persistent CTAs walk the device-built tile
 // list of tc_sched.cuh; every wait is bounded (timeout -> status word).
 #include <cuda.h>
 
@@ -47,8 +49,9 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kN4Threads = 448;
-constexpr int kN4Epi = 256;                   // warps 2-9
+constexpr int kN4EpiWarps = 16;               // warps 2-17
+constexpr int kN4Epi = 32 * kN4EpiWarps;
+constexpr int kN4Threads = 64 + kN4Epi + 128;
 constexpr int kN4BK = 128;                    // bytes of packed codes per row and stage (256 K elements)
 constexpr int kN4BM = 128;                    // weight rows per tile = MMA M
 constexpr uint32_t kN4ACodes = kN4BM * kN4BK;     // 16 KB of codes per weight tile and stage
@@ -274,8 +277,8 @@ ffn_nvf4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       int no_abort = 0;
       mbar_wait(smem_u32(&c->drain), 0, &no_abort, kN4DrainNs);
     }
-  } else if (warp >= 10) {
-    // -------------------------------------------------- block-scale writers (warps 10..13)
+  } else if (warp >= 2 + kN4EpiWarps) {
+    // -------------------------------------------------- block-scale writers (warps 18..21)
     // Warp w writes the lanes of TMEM quadrant q = w % 4.  Column map of a
     // stage's 48 scale columns: weight tile a (0 = gate / down, 1 = up) at
     // 16 a + 4 kk + q for weight row m = 32 q + lane; activations at
@@ -328,9 +331,10 @@ ffn_nvf4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       if (!ok) break;
     }
   } else {
-    // -------------------------------------------------- epilogue (warps 2..9)
+    // -------------------------------------------------- epilogue (warps 2..17)
     const int sub = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;               // 0..3: splits the column chunks
+    constexpr int kParts = kN4EpiWarps / 4;
     const int n = sub * 32 + lane;                  // weight row within the tile
     const int et = threadIdx.x - 64;                // 0..255
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
@@ -369,10 +373,10 @@ ffn_nvf4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       const int col = t.wt * kN4BM + n;
       if (MODE == 1) {
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
-        constexpr int TPC = 32 / TERMS;             // tokens per 32-column chunk
-        for (int c0 = 32 * half; c0 < N; c0 += 64) {
-          float gv[32], uv[32];
-          tmem_ld32x2(cb + c0, cb + N + c0, gv, uv);
+        constexpr int TPC = 16 / TERMS;             // tokens per 16-column chunk
+        for (int c0 = 16 * part; c0 < N; c0 += 16 * kParts) {
+          float gv[16], uv[16];
+          tmem_ld16x2(cb + c0, cb + N + c0, gv, uv);
 #pragma unroll
           for (int jj = 0; jj < TPC; ++jj) {
             const int j = c0 / TERMS + jj;
@@ -392,10 +396,10 @@ ffn_nvf4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * N);
         void* outp = shr ? a.shared_out : a.out_perm;
         const size_t out0 = static_cast<size_t>(shr ? t.row0 - a.P : t.row0) * a.d + col;
-        constexpr int TPC = 64 / TERMS;             // tokens per 64-column chunk
-        for (int c0 = 64 * half; c0 < N; c0 += 128) {
-          float d0[32], d1[32];
-          tmem_ld32x2(cb + c0, cb + c0 + 32, d0, d1);
+        constexpr int TPC = 32 / TERMS;             // tokens per 32-column chunk
+        for (int c0 = 32 * part; c0 < N; c0 += 32 * kParts) {
+          float d0[16], d1[16];
+          tmem_ld16x2(cb + c0, cb + c0 + 16, d0, d1);
 #pragma unroll
           for (int jj = 0; jj < TPC; ++jj) {
             const int j = c0 / TERMS + jj;
@@ -404,7 +408,7 @@ ffn_nvf4_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
 #pragma unroll
               for (int tt = 0; tt < TERMS; ++tt) {
                 const int q = jj * TERMS + tt;
-                v += (q < 32 ? d0[q] : d1[q - 32]) * coef[c0 + q];
+                v += (q < 16 ? d0[q] : d1[q - 16]) * coef[c0 + q];
               }
               store_out(outp, out0 + static_cast<size_t>(j) * a.d, v, a.out_bf16);
             }
@@ -662,9 +666,9 @@ cudaError_t launch_n4_gemm(const CUtensorMap& mA, const CUtensorMap& mAS, const 
   const int stage_bytes = NA * kN4ACodes + b_slot + (NA + 1) * kN4Sf;
   a.stages = std::min(kN4MaxStages, kN4SmemBudget / stage_bytes);
   // TMEM: accumulators (double-buffered when they fit), then kN4SfCols scale
-  // columns per stage.  The epilogue's 32-column loads may reach up to 31
-  // columns past an accumulator (gemm1: gate at c0 and up at N + c0; gemm2:
-  // 64 columns from c0); the scale region starts after that reach.
+  // columns per stage.  The epilogue's loads (gemm1: 16 columns at c0 and at
+  // N + c0; gemm2: 32 from c0) stay within the rounded reach below, after
+  // which the scale region starts.
   const int per_acc = NA * N;
   auto sf_start = [&](int bufs) {
     const int acc_end = bufs * per_acc;
