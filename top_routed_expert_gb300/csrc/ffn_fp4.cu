@@ -13,11 +13,13 @@
 // weight scale and the row scale (times the gate weight in the down
 // projection) are applied in the epilogue.
 //
-// Gate/up tiles interleave the two projections: the 128 weight rows of a
-// tile are, per 32-row TMEM sub-partition, 16 gate rows and the 16 up rows of
-// the same features (64 features per tile), so one accumulator holds both,
-// two of them fit TMEM at 256 tokens, and an epilogue lane pairs gate with
-// up through one exchange with the lane 16 away.
+// Large token tiles (128 or more) interleave the two gate/up projections in
+// one weight tile (IL): its 128 rows are, per 32-row TMEM sub-partition, 16
+// gate rows and the 16 up rows of the same features (64 features per tile),
+// so one accumulator holds both, two of them fit TMEM at 256 tokens, and an
+// epilogue lane pairs gate with up through one exchange with the lane 16
+// away.  Smaller tiles keep a gate tile and an up tile of 128 features each
+// (two accumulators), which measured faster at decode.
 //
 // Warp roles (480 threads): warp 0 issues the TMA loads of the activation
 // tiles into a ring of their own (up to 8 slots, so that the small decode
@@ -188,25 +190,26 @@ __device__ __forceinline__ void cursor_next(KbCursor& cu, const GroupTable& gt, 
 }
 
 // First row (within its tensor map: routed or shared weights) of this tile's
-// weights, and its K: gate/up -- the tile's 64 gate rows (a_idx = 0) or its
-// 64 up rows (a_idx = 1); down -- its 128 rows.
-template <int MODE>
+// weights, and its K: gate/up -- the tile's gate rows (a_idx = 0) or its up
+// rows (a_idx = 1), 64 of each when interleaved, else 128; down -- its 128 rows.
+template <int MODE, bool IL>
 __device__ __forceinline__ int weight_row(const F4Args& a, const Tile& t, int a_idx, int* K) {
   const bool shr = t.g == a.E;
   if (MODE == 1) {
     const int width = shr ? a.fs : a.f;
     *K = a.d;
-    return (shr ? 0 : t.g * 2 * a.f) + (a_idx ? width : 0) + t.wt * (kF4BM / 2);
+    return (shr ? 0 : t.g * 2 * a.f) + (a_idx ? width : 0) + t.wt * (IL ? kF4BM / 2 : kF4BM);
   }
   *K = shr ? a.fs : a.f;
   return (shr ? 0 : t.g * a.d) + t.wt * kF4BM;
 }
 
-template <int MODE>
+template <int MODE, bool IL>
 __global__ void __launch_bounds__(kF4Threads, 1)
 ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapA,
                const __grid_constant__ CUtensorMap mapAs, F4Args a) {
-  constexpr int NA = 1;   // one weight tile per stage (gate/up interleaved in it)
+  constexpr bool GU_IL = IL && MODE == 1;
+  constexpr int NA = (MODE == 1 && !GU_IL) ? 2 : 1;   // weight tiles per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int N = a.TN;                                   // one f16 column per token
@@ -244,12 +247,14 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
     fence_barrier_init();
   }
   pdl_enter();   // from here on the kernel reads what earlier kernels wrote
-  if (MODE == 1)   // 64 features per tile
+  if (MODE == 1) {   // 64 features per tile when interleaved, else 128
+    constexpr int WT = GU_IL ? kF4BM / 2 : kF4BM;
     build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN,
-                      a.routed_on ? a.f / (kF4BM / 2) : 0, a.shared_on ? a.fs / (kF4BM / 2) : 0, a.status);
-  else
+                      a.routed_on ? a.f / WT : 0, a.shared_on ? a.fs / WT : 0, a.status);
+  } else {
     build_group_table(c->gt, a.routed_on ? a.offsets : nullptr, a.E, a.P, a.T, a.TN,
                       a.routed_on ? a.d / kF4BM : 0, a.shared_on ? a.d / kF4BM : 0, a.status);
+  }
   if (warp == 1) {
     tmem_alloc(smem_u32(&c->tmem_base), a.tmem_cols);
     tmem_relinquish();
@@ -297,6 +302,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
         if (!mbar_wait(smem_u32(&c->tempty[ab]), aph ^ 1u, abort, kF4WaitNs)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + static_cast<uint32_t>(ab * NA * N);
+        const uint32_t d1 = d0 + static_cast<uint32_t>(N);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(smem_u32(&c->bfull[bs]), bph, abort, kF4WaitNs) ||
               !mbar_wait(smem_u32(&c->aready[st]), ph, abort, kF4WaitNs)) {
@@ -306,11 +312,13 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + st * stage_bytes);
           const uint64_t da0 = desc_sw128(sA);
+          const uint64_t da1 = desc_sw128(sA + kF4ATile);
           const uint64_t db = desc_sw128(smem_u32(bring + bs * b_slot));
 #pragma unroll
           for (int kk = 0; kk < kF4BK / 16; ++kk) {
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             mma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, accum);
+            if (NA == 2) mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, accum);
           }
           mma_commit(smem_u32(&c->empty[st]));
           mma_commit(smem_u32(&c->bempty[bs]));
@@ -370,7 +378,22 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
       if (!mbar_wait_sleep(smem_u32(&c->tfull[ab]), aph, abort, kF4WaitNs, kF4IdleSleepNs)) break;
       tc_fence_after();
       const int col = t.wt * kF4BM + n;
-      if (MODE == 1) {
+      if constexpr (MODE == 1 && !GU_IL) {
+        const uint32_t cb = tmem + lane_off + static_cast<uint32_t>(ab * 2 * N);
+        for (int c0 = 0; c0 < N; c0 += 16) {       // 16 tokens per chunk
+          float gv[16], uv[16];
+          tmem_ld16x2(cb + c0, cb + N + c0, gv, uv);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = c0 + jj;
+            if (j < t.nrows) {
+              const float cf = coef[j];
+              a.h[static_cast<size_t>(t.row0 + j) * a.fmax + col] =
+                  __float2bfloat16_rn(silu(gv[jj] * cf) * (uv[jj] * cf));
+            }
+          }
+        }
+      } else if constexpr (MODE == 1) {
         // lanes 0-15 hold gate, lanes 16-31 up, of features fb .. fb+15; per
         // 32-column chunk lane l < 16 finishes tokens c0 .. c0+15 and lane
         // l + 16 tokens c0+16 .. c0+31 after one exchange
@@ -425,12 +448,13 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
     }
   } else if (warp < 6 + kF4ConvWarps) {
     // -------------------------------------------------- weight converters (warps 6..13)
-    // two threads per raw row, four 16-byte f16 chunks each
+    // two weight tiles (gate and up, not interleaved): thread -> one row of
+    // one tile; one tile: two threads per row, four 16-byte f16 chunks each
     const int ct = threadIdx.x - 192;                 // 0..255
     const int r = ct & (kF4BM - 1);
-    constexpr int ai = 0;
-    constexpr int kChunks = 4;                        // f16 chunks (8 elements) per thread and stage
-    const int c_lo = 4 * (ct >> 7);
+    const int ai = (NA == 2) ? (ct >> 7) : 0;
+    constexpr int kChunks = (NA == 2) ? 8 : 4;        // f16 chunks (8 elements) per thread and stage
+    const int c_lo = (NA == 2) ? 0 : 4 * (ct >> 7);
     const int sw = (r >> 1) & 3;                      // 64-byte swizzle of the raw code rows
     KbCursor conv;
     cursor_begin<MODE>(conv, c->gt, G, total, a);
@@ -448,7 +472,7 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
       // 32 q + i holds gate feature 16 q + i (i < 16), 32 q + 16 + i up
       // feature 16 q + i (r and its tile row agree mod 16, so the swizzle is
       // the same)
-      const int rd = (MODE == 1) ? ((r & 63) >> 4) * 32 + (r >> 6) * 16 + (r & 15) : r;
+      const int rd = GU_IL ? ((r & 63) >> 4) * 32 + (r >> 6) * 16 + (r & 15) : r;
       uint8_t* dst_row = smem + st * stage_bytes + ai * kF4ATile + rd * 128;
 #pragma unroll
       for (int q = 0; q < kChunks / 4; ++q) {
@@ -498,25 +522,45 @@ ffn_fp4_kernel(const __grid_constant__ CUtensorMap mapB, const __grid_constant__
       const uint32_t slot = smem_u32(raw + rs * raw_slot);
       const uint32_t bar = smem_u32(&c->rfull[rs]);
       const int rb = cu.kb >> 1;                      // raw block within the row
-      // gate/up: two boxes of 64 rows (gate, then up) fill the slot's 128
-      // raw rows; down: one box of 128 rows
-      constexpr int kParts = (MODE == 1) ? 2 : 1;
-      constexpr int kRowsPer = kF4BM / kParts;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar, kF4RawCodes);
-        for (int p2 = 0; p2 < kParts; ++p2) {
-          int K;
-          const int row = weight_row<MODE>(a, cu.t, p2, &K);
-          tma_load_2d(slot + p2 * kRowsPer * (kF4RK / 2), shr ? &mapAs : &mapA, rb * (kF4RK / 2), row, bar);
+      if constexpr (GU_IL) {
+        // two boxes of 64 rows (gate, then up) fill the slot's 128 raw rows
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, kF4RawCodes);
+          for (int p2 = 0; p2 < 2; ++p2) {
+            int K;
+            const int row = weight_row<MODE, IL>(a, cu.t, p2, &K);
+            tma_load_2d(slot + p2 * (kF4BM / 2) * (kF4RK / 2), shr ? &mapAs : &mapA, rb * (kF4RK / 2), row, bar);
+          }
         }
-      }
 #pragma unroll
-      for (int j = 0; j < kF4BM / 32; ++j) {
-        const int rr = lane + 32 * j;
-        int K;
-        const int row = weight_row<MODE>(a, cu.t, rr / kRowsPer, &K) + rr % kRowsPer;
-        const uint8_t* sc = (shr ? a.ssc : a.wsc) + static_cast<size_t>(row) * (K / 16) + rb * (kF4RK / 16);
-        cp_async8(slot + kF4RawCodes + rr * (kF4RK / 16), sc);
+        for (int j = 0; j < kF4BM / 32; ++j) {
+          const int rr = lane + 32 * j;
+          int K;
+          const int row = weight_row<MODE, IL>(a, cu.t, rr / (kF4BM / 2), &K) + rr % (kF4BM / 2);
+          const uint8_t* sc = (shr ? a.ssc : a.wsc) + static_cast<size_t>(row) * (K / 16) + rb * (kF4RK / 16);
+          cp_async8(slot + kF4RawCodes + rr * (kF4RK / 16), sc);
+        }
+      } else {
+        // one box of 128 rows per weight tile
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, NA * kF4RawCodes);
+          for (int t2 = 0; t2 < NA; ++t2) {
+            int K;
+            const int row = weight_row<MODE, IL>(a, cu.t, t2, &K);
+            tma_load_2d(slot + t2 * kF4RawCodes, shr ? &mapAs : &mapA, rb * (kF4RK / 2), row, bar);
+          }
+        }
+        for (int t2 = 0; t2 < NA; ++t2) {
+          int K;
+          const int row = weight_row<MODE, IL>(a, cu.t, t2, &K);
+          const uint8_t* sc = (shr ? a.ssc : a.wsc) + static_cast<size_t>(row) * (K / 16) + rb * (kF4RK / 16);
+#pragma unroll
+          for (int j = 0; j < kF4BM / 32; ++j) {
+            const int rr = lane + 32 * j;
+            cp_async8(slot + NA * kF4RawCodes + t2 * kF4RawScales + rr * (kF4RK / 16),
+                      sc + static_cast<size_t>(rr) * (K / 16));
+          }
+        }
       }
       cp_async_arrive_noinc(bar);
       pending |= 1u << rs;
@@ -702,10 +746,10 @@ F4Plan f4_plan(const moe_config_t& c) {
   return p;
 }
 
-template <int MODE>
+template <int MODE, bool IL>
 cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const CUtensorMap& mAs, F4Args a,
                            int wtiles_routed, int wtiles_shared, int grid_cap, cudaStream_t stream) {
-  constexpr int NA = 1;   // one (gate/up interleaved, or down) weight tile per stage
+  constexpr int NA = (MODE == 1 && !IL) ? 2 : 1;   // weight tiles per stage
   const int N = a.TN;
   const int stage_bytes = NA * kF4ATile;
   const int b_slot = static_cast<int>(align_up(static_cast<size_t>(N) * 128, 1024));
@@ -723,9 +767,10 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
   if (a.raw_slots < 2) return cudaErrorInvalidConfiguration;
   const int per_acc = NA * N;
   a.acc_bufs = (2 * per_acc <= 512) ? 2 : 1;
-  // epilogue loads: 32 columns at c0, c0 < N in steps of 32
+  // epilogue loads: 32 columns at c0 (c0 < N, steps of 32), or, two gate/up
+  // accumulators, 16 columns at c0 and at N + c0
   const int last = (a.acc_bufs - 1) * per_acc;
-  const int reach = last + (N + 31) / 32 * 32;
+  const int reach = (NA == 2) ? last + N + (N + 15) / 16 * 16 : last + (N + 31) / 32 * 32;
   int cols = 32;
   while (cols < reach) cols *= 2;
   if (cols > 512) return cudaErrorInvalidConfiguration;
@@ -734,13 +779,14 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
                 static_cast<size_t>(a.raw_slots) * raw_slot + sizeof(F4Ctrl);
   smem = std::max<size_t>(smem, 120 * 1024);   // one CTA per SM: TMEM is never contended
   if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
-  cudaError_t err = ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_fp4_kernel<MODE>), static_cast<int>(smem));
+  cudaError_t err =
+      ensure_kernel_attrs(reinterpret_cast<const void*>(ffn_fp4_kernel<MODE, IL>), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const long long tiles_ub = (a.routed_on ? static_cast<long long>(wtiles_routed) * (a.P / a.TN + a.E) : 0) +
                              (a.shared_on ? static_cast<long long>(wtiles_shared) * ((a.T + a.TN - 1) / a.TN) : 0);
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(grid_cap, tiles_ub)));
   count_launches(1);
-  return launch_pdl(ffn_fp4_kernel<MODE>, grid, kF4Threads, smem, stream, mB, mA, mAs, a);
+  return launch_pdl(ffn_fp4_kernel<MODE, IL>, grid, kF4Threads, smem, stream, mB, mA, mAs, a);
 }
 
 }  // namespace
@@ -789,15 +835,18 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   a.status = status;
 
   CUtensorMap mB, mA, mAs;
-  // gemm1: gate / up
+  // gemm1: gate / up; token tiles of 128 or more interleave gate and up
+  const bool il = a.TN >= 128;
+  const uint32_t abox = il ? kF4BM / 2 : kF4BM;
   if (!make_f16_map(&mB, xh, R, d, d, a.TN) ||
-      !make_code_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, kF4BM / 2) ||
-      !make_code_map(&mAs, w->s13, 2 * static_cast<uint64_t>(fs), d, kF4BM / 2))
+      !make_code_map(&mA, w->w13, static_cast<uint64_t>(E) * 2 * f, d, abox) ||
+      !make_code_map(&mAs, w->s13, 2 * static_cast<uint64_t>(fs), d, abox))
     return cudaErrorInvalidValue;
   a.wsc = static_cast<const uint8_t*>(w->w13_scale); a.wg = w->w13_gscale;
   a.ssc = static_cast<const uint8_t*>(w->s13_scale); a.sg = w->s13_gscale;
   a.b_scale = sx;
-  err = launch_f4_gemm<1>(mB, mA, mAs, a, f / (kF4BM / 2), fs / (kF4BM / 2), cap, stream);
+  err = il ? launch_f4_gemm<1, true>(mB, mA, mAs, a, f / abox, fs / abox, cap, stream)
+           : launch_f4_gemm<1, false>(mB, mA, mAs, a, f / abox, fs / abox, cap, stream);
   if (err != cudaSuccess) return err;
 
   count_launches(1);
@@ -814,7 +863,7 @@ cudaError_t launch_ffn_fp4(const moe_config_t& c, const void* x, const float* to
   a.wsc = static_cast<const uint8_t*>(w->w2_scale); a.wg = w->w2_gscale;
   a.ssc = static_cast<const uint8_t*>(w->s2_scale); a.sg = w->s2_gscale;
   a.b_scale = sh;
-  return launch_f4_gemm<2>(mB, mA, mAs, a, d / kF4BM, d / kF4BM, cap, stream);
+  return launch_f4_gemm<2, false>(mB, mA, mAs, a, d / kF4BM, d / kF4BM, cap, stream);
 }
 
 }  // namespace moe
