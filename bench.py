@@ -501,7 +501,7 @@ def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_ter
                               f"{act_terms}x the layer's FLOPs at the FP4 rate")}
         elif act_terms == 2:
             issued = {"tflops": 2.0 * alg["ffn_flops"] / ffn_s / 1e12, "peak": 2.0 * bf16,
-                      "how": "two E4M3 terms per activation: kind::f8f6f4 MMAs issue 2x the FLOPs"}
+                      "how": "two E4M3 terms per activation: the FP8 MMAs (kind::f8f6f4, or block-scaled kind::mxf8f6f4 on CTA pairs) issue 2x the FLOPs"}
         else:
             issued = {"tflops": alg["ffn_flops"] / ffn_s / 1e12, "peak": 2.0 * bf16,
                       "how": "one E4M3 term per activation (MOE_FLAG_ACT_E4M3): the MMAs issue the layer's FLOPs"}
