@@ -324,6 +324,7 @@ def test_tensor_core_path_tiles(shape, w_dtype):
 PAIR_SHAPES = [
     dict(T=200, d=512, E=16, k=4, f=256, fs=512),    # 50 rows / expert: TN 64 (gate/up), 128 (down)
     dict(T=777, d=768, E=8, k=2, f=512, fs=256),     # 194 rows / expert, 3 down tiles of 256 rows
+    dict(T=203, d=256, E=2, k=1, f=256, fs=256),     # 101 rows / expert, k = 1, one weight tile per group
 ]
 
 
