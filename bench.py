@@ -228,6 +228,19 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
+# flags that change which kernels (or how many bytes) the expert stage runs
+TRAFFIC_VARIANT_FLAGS = ("MOE_FLAG_SIMT_FFN", "MOE_FLAG_BF16_EXPERT_OUT", "MOE_FLAG_ACT_E4M3", "MOE_FLAG_ACT_NVFP4",
+                         "MOE_FLAG_NVFP4_F16")
+
+
+def traffic_key(workload, flags):
+    """Key of a workload's DRAM-traffic record: the workload name, plus every
+    kernel-changing flag that is set (records exist for the default flags)."""
+    from top_routed_expert_gb300 import abi
+    on = [n for n in TRAFFIC_VARIANT_FLAGS if flags & getattr(abi, n)]
+    return "+".join([workload] + on)
+
+
 def recorded_traffic(workload, kernel):
     """dram bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources (else None)."""
@@ -458,7 +471,8 @@ def nvfp4_on_f16_path(cfg, flags):
     return cfg.T * cfg.k > 16 * cfg.E
 
 
-def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_terms=None, nvfp4_f16=False):
+def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_terms=None, nvfp4_f16=False,
+             traffic_key=None):
     """Roofline of the dominant stage (moe_expert_ffn) and of the whole layer.
 
     HBM bound: algorithmic bytes at the measured copy bandwidth.  Tensor
@@ -507,7 +521,9 @@ def roofline(alg, ms_ffn, ms_step, workload, w_dtype="e4m3", simt=False, act_ter
                       "how": "one E4M3 term per activation (MOE_FLAG_ACT_E4M3): the MMAs issue the layer's FLOPs"}
         issued["frac"] = issued["tflops"] / issued["peak"]
         roof["issued"] = issued
-    roof["traffic"] = recorded_traffic(workload, roof["kernel"])
+    # a variant (a flag that changes the kernels) has no record unless one was
+    # captured under its own key
+    roof["traffic"] = recorded_traffic(traffic_key or workload, roof["kernel"])
     t_layer_roof = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (tc_peak * 1e12))
     return roof, t_layer_roof / (ms_step / 1e3)
 
@@ -666,7 +682,7 @@ def run_ours(args, world, rank, local):
                 g1, _ = time_graph(l1, xp, steps, args.warmup, world, dev, torch, None)
             f16 = nvfp4_f16 or (src.cfg.w_dtype == "nvfp4" and nvfp4_on_f16_path(src.cfg, lay.flags))
             rp, lfp = roofline(mp["alg"], mp["stage_ms"]["expert_ffn"], gp, name, src.cfg.w_dtype, args.simt,
-                               act_terms, f16)
+                               act_terms, f16, traffic_key(name, lay.flags))
             out = {"workload": WORKLOAD_TEXT[name], "value": job_value(world, src.cfg.T, gp), "unit": "tokens/s",
                    "ms_per_step": gp, "steps": steps, "roofline": rp, "layer_roofline_frac": lfp,
                    "active_experts": mp["alg"]["active"],
@@ -730,7 +746,8 @@ def run_ours(args, world, rank, local):
     value = job_value(world, T, graph_ms)
     roof, layer_frac = roofline(m["alg"], m["stage_ms"]["expert_ffn"], graph_ms, args.workload, cfg.w_dtype,
                                 args.simt, 1 if args.act_e4m3 else None,
-                                cfg.w_dtype == "nvfp4" and nvfp4_on_f16_path(cfg, flags))
+                                cfg.w_dtype == "nvfp4" and nvfp4_on_f16_path(cfg, flags),
+                                traffic_key(args.workload, flags))
     cpu = None
     if not args.no_cpu_baseline and world == 1:   # the oracle baseline: rank 0 of a single-GPU run only
         v, n, el = time_oracle(inp, args.cpu_budget)

@@ -87,3 +87,16 @@ def test_nvfp4_path_choice_follows_the_library():
     pre = NS(T=8192, k=8, E=128)
     assert not bench.nvfp4_on_f16_path(dec, 0) and bench.nvfp4_on_f16_path(pre, 0)
     assert bench.nvfp4_on_f16_path(dec, 0x20) and not bench.nvfp4_on_f16_path(pre, 0x10)
+
+
+def test_traffic_records_are_per_variant():
+    """A flag that changes the expert-stage kernels gets no traffic record
+    recorded for the default path of the same workload."""
+    import bench
+    from top_routed_expert_gb300 import abi
+    assert bench.traffic_key("prefill", 0) == "prefill"
+    assert bench.traffic_key("prefill", abi.MOE_FLAG_ACT_E4M3) == "prefill+MOE_FLAG_ACT_E4M3"
+    assert bench.traffic_key("100b_decode", abi.MOE_FLAG_NVFP4_F16 | abi.MOE_FLAG_NO_OVERLAP) == \
+        "100b_decode+MOE_FLAG_NVFP4_F16"
+    k = "moe_expert_ffn (grouped SwiGLU GEMMs + shared expert)"
+    assert bench.recorded_traffic(bench.traffic_key("100b_prefill", abi.MOE_FLAG_ACT_NVFP4), k) is None
