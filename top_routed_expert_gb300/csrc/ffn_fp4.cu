@@ -56,7 +56,7 @@ constexpr int kF4BM = 128;                  // weight rows per tile
 constexpr uint32_t kF4ATile = kF4BM * 128;  // 16 KB f16 tile
 constexpr uint32_t kF4RawCodes = kF4BM * (kF4RK / 2);    // 8 KB of packed codes per weight tile
 constexpr uint32_t kF4RawScales = kF4BM * (kF4RK / 16);  // 1 KB of block scales per weight tile
-constexpr int kF4MaxStages = 3;
+constexpr int kF4MaxStages = 5;
 constexpr int kF4MaxB = 8;
 constexpr int kF4MaxRaw = 16;
 constexpr uint64_t kF4WaitNs = 2000000000ull;
@@ -758,8 +758,10 @@ cudaError_t launch_f4_gemm(const CUtensorMap& mB, const CUtensorMap& mA, const C
   // at most 8); the rest of the budget goes to the raw ring, which hides HBM
   // latency
   // (256-token gate/up tiles: two 32 KB activation slots, so that three raw
-  // slots still fit)
-  a.stages = kF4MaxStages;
+  // slots still fit).  Tiles of 128 tokens or more keep five f16 weight
+  // stages (converters and MMA then wait on each other less), smaller ones
+  // three and more raw slots
+  a.stages = N >= 128 ? 5 : 3;
   a.bslots = std::max(3, std::min(kF4MaxB, 32768 / b_slot));
   auto raw_fit = [&] { return (kF4SmemBudget - a.stages * stage_bytes - a.bslots * b_slot) / raw_slot; };
   while (raw_fit() < 3 && a.bslots > 2) --a.bslots;
