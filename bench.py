@@ -219,10 +219,12 @@ def cores():
 
 # ------------------------------------------------------------------ traffic record
 
-def source_hash():
+def source_hash(files=None):
+    """Hash of the kernel sources a record was measured on: the listed files
+    of csrc/ (every file when None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_routed_expert_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in sorted(files if files is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, fn), "rb") as fh:
             h.update(fn.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -243,14 +245,21 @@ def traffic_key(workload, flags):
 
 def recorded_traffic(workload, kernel):
     """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current sources of the kernels it covers (a record lists them under
+    "sources"; without the list, every kernel source counts), else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         rec = json.load(fh)
     r = rec.get(workload, {})
-    if r.get("kernel") != kernel or r.get("source_hash") != source_hash():
+    if r.get("kernel") != kernel:
+        return None
+    try:
+        current = source_hash(r.get("sources"))
+    except OSError:                      # a listed source no longer exists
+        return None
+    if r.get("source_hash") != current:
         return None
     return r.get("dram_bytes_per_launch")
 

@@ -100,3 +100,27 @@ def test_traffic_records_are_per_variant():
         "100b_decode+MOE_FLAG_NVFP4_F16"
     k = "moe_expert_ffn (grouped SwiGLU GEMMs + shared expert)"
     assert bench.recorded_traffic(bench.traffic_key("100b_prefill", abi.MOE_FLAG_ACT_NVFP4), k) is None
+
+
+def test_traffic_records_name_their_sources():
+    """Each DRAM-traffic record lists the kernel sources it was measured on;
+    a change to one of them (a different hash) retires the record."""
+    import bench
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    csrc = os.path.join(bench.ROOT, "top_routed_expert_gb300", "csrc")
+    for name, r in rec.items():
+        assert r["sources"], name
+        for fn in r["sources"]:
+            assert os.path.exists(os.path.join(csrc, fn)), (name, fn)
+        assert len(r["source_hash"]) == 16 and int(r["source_hash"], 16) >= 0
+        assert r["dram_bytes_per_launch"] > 0
+
+
+def test_traffic_record_retired_when_its_sources_change(monkeypatch):
+    import bench
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    r = rec["decode"]
+    monkeypatch.setattr(bench, "source_hash", lambda files=None: r["source_hash"])
+    assert bench.recorded_traffic("decode", r["kernel"]) == r["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "source_hash", lambda files=None: "0" * 16)
+    assert bench.recorded_traffic("decode", r["kernel"]) is None
