@@ -50,7 +50,7 @@ def test_traffic_only_for_matching_sources(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "source_hash", lambda: "abc")
+    monkeypatch.setattr(bench, "source_hash", lambda files=None: "abc")
     rec = {"decode": {"kernel": kernel, "source_hash": "abc", "dram_bytes_per_launch": 123}}
     (prof / "traffic.json").write_text(json.dumps(rec))
     assert bench.recorded_traffic("decode", kernel) == 123
