@@ -13,7 +13,7 @@ import oracle
 from top_routed_expert_gb300 import abi
 from top_routed_expert_gb300.layer import MoELayer
 
-from .gpu_util import check_output, check_routing, device_x, oracle_y, run_layer, workload
+from .gpu_util import LOSSY_MAX_ABS_RMS, check_output, check_routing, device_x, oracle_y, run_layer, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -336,6 +336,16 @@ def test_cta_pair_tiles(shape, act):
     _, _, y, ids, w, offs = run_layer(inp, flags)
     check_routing(inp, ids, w, offs)
     check_output(inp, y, ids, act=act)
+
+
+def test_cta_pair_bf16_expert_outputs():
+    # the pair down projection's bf16 store branch: one more bf16 rounding of
+    # each expert output (about 2^-9 relative), hence the wider element bound
+    shape = PAIR_SHAPES[0]
+    inp = moe_synth.make_custom(x_dtype="bf16", w_dtype="e4m3", seed=shape["T"] + 5, **shape)
+    _, _, y, ids, w, offs = run_layer(inp, abi.MOE_FLAG_BF16_EXPERT_OUT)
+    check_routing(inp, ids, w, offs)
+    check_output(inp, y, ids, max_abs_rms=LOSSY_MAX_ABS_RMS)
 
 
 @pytest.mark.parametrize("name", ["decode", "100b_decode"])
